@@ -1,0 +1,165 @@
+"""Checks that pin the CPU oracle to facts other than itself.
+
+Each ``pin_*`` takes a ``head`` callable with the signature of
+``oracle.Oracle.head`` and raises AssertionError when the oracle disagrees
+with a worked example, an identity of the method, a closed form, a library
+routine or a finite-difference derivative.  ``test_oracle.py`` runs them on the
+real oracle; ``test_oracle_mutants.py`` runs them on copies of the oracle with a
+planted mistake and requires that each mistake trips at least one pin.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+from scipy.special import logsumexp, softmax
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _close(a, b, tol, what):
+    a, b = np.asarray(a, dtype=np.float64), np.asarray(b, dtype=np.float64)
+    if a.shape != b.shape:
+        raise AssertionError(f"{what}: shape {a.shape} != {b.shape}")
+    if not np.all(np.isfinite(a)):
+        raise AssertionError(f"{what}: non-finite values")
+    err = float(np.max(np.abs(a - b))) if a.size else 0.0
+    if err > tol:
+        raise AssertionError(f"{what}: max abs err {err:.3e} > {tol:.3e}")
+
+
+def _rand(rng, S, hd, std=1.0):
+    return rng.standard_normal((S, hd)) * std
+
+
+def pin_hand_2x2(head):
+    """The 2x2 example worked by hand from the page formulas (tests/golden/hand_2x2.json)."""
+    with open(os.path.join(GOLDEN, "hand_2x2.json")) as f:
+        g = json.load(f)
+    r = head(np.array(g["q"], float), np.array(g["k"], float), np.array(g["v"], float),
+             np.array(g["dout"], float), g["scale"], g["causal"], diagnostics=True)
+    e = g["expect"]
+    lse = [1.0, 1.0 + math.log(2.0)]
+    _close(r["out"], e["out"], 1e-14, "2x2 out")
+    _close(r["lse"], lse, 1e-14, "2x2 lse")
+    _close(r["dq"], e["dq"], 1e-14, "2x2 dq")
+    _close(r["dk"], e["dk"], 1e-14, "2x2 dk")
+    _close(r["dv"], e["dv"], 1e-14, "2x2 dv")
+    _close(r["pdp_rowsum"], e["D"], 1e-14, "2x2 D")
+
+
+def _masked_scores(q, k, scale):
+    S = q.shape[0]
+    s = scale * (q @ k.T)
+    s[np.triu(np.ones((S, S), bool), 1)] = -np.inf
+    return s
+
+
+def pin_row_identities(head, shapes=((1, 4), (7, 3), (33, 8), (70, 16)), seeds=(1, 2)):
+    """Identities of the method on random inputs:
+    sum_j P_ij = 1; sum_j P_ij dP_ij = dO_i . O_i (the D_i of the flash backward);
+    sum_j dS_ij = 0; sum_j dK_j = 0 (O is invariant to K -> K + 1 c^T under the
+    causal window); dQ_0 = 0, O_0 = V_0, L_0 = s_00 (row 0 sees one key);
+    dV_{S-1} = P_{S-1,S-1} dO_{S-1} (the last key is seen by the last row only);
+    L_i = logsumexp of the masked row (scipy)."""
+    for seed in seeds:
+        rng = np.random.default_rng(seed)
+        for S, hd in shapes:
+            q, k, v, do = (_rand(rng, S, hd) for _ in range(4))
+            scale = 1.0 / math.sqrt(hd)
+            r = head(q, k, v, do, scale, True, diagnostics=True)
+            tag = f"S={S} hd={hd} seed={seed}"
+            _close(r["p_rowsum"], np.ones(S), 1e-12, f"sum_j P {tag}")
+            D = np.sum(do * r["out"], axis=1)
+            _close(r["pdp_rowsum"], D, 1e-11 * max(1.0, np.max(np.abs(D))), f"sum_j P dP = dO.O {tag}")
+            _close(r["ds_rowsum"], np.zeros(S), 1e-12, f"sum_j dS {tag}")
+            _close(np.sum(r["dk"], axis=0), np.zeros(hd), 1e-11 * S, f"sum_j dK {tag}")
+            _close(r["dq"][0], np.zeros(hd), 1e-14, f"dQ_0 {tag}")
+            _close(r["out"][0], v[0], 1e-13, f"O_0 {tag}")
+            s = _masked_scores(q, k, scale)
+            _close(r["lse"][0], s[0, 0], 1e-13, f"L_0 {tag}")
+            p_last = math.exp(s[S - 1, S - 1] - r["lse"][S - 1])
+            _close(r["dv"][S - 1], p_last * do[S - 1], 1e-12, f"dV_last {tag}")
+            _close(r["lse"], logsumexp(s, axis=1), 1e-12, f"L vs scipy logsumexp {tag}")
+
+
+def pin_dense_library(head, shapes=((5, 3), (40, 8)), seed=3):
+    """Without the mask the forward is dense softmax attention: compare with
+    scipy's softmax/logsumexp and numpy matmul."""
+    rng = np.random.default_rng(seed)
+    for S, hd in shapes:
+        q, k, v = (_rand(rng, S, hd) for _ in range(3))
+        scale = 0.7
+        r = head(q, k, v, None, scale, False)
+        s = scale * (q @ k.T)
+        _close(r["out"], softmax(s, axis=1) @ v, 1e-12, f"dense out S={S}")
+        _close(r["lse"], logsumexp(s, axis=1), 1e-12, f"dense lse S={S}")
+
+
+def pin_special_cases(head):
+    """Closed forms: S=1 gives O=V, L = scale q.k, dQ = dK = 0, dV = dO;
+    Q=0 gives causal running means O_i = mean_{j<=i} V_j with L_i = ln(i+1);
+    hd=1 against a pure-Python scalar softmax."""
+    rng = np.random.default_rng(11)
+    q, k, v, do = (_rand(rng, 1, 5) for _ in range(4))
+    r = head(q, k, v, do, 0.3, True)
+    _close(r["out"], v, 1e-15, "S=1 out")
+    _close(r["lse"], [0.3 * float(q[0] @ k[0])], 1e-14, "S=1 lse")
+    _close(r["dq"], np.zeros((1, 5)), 0.0, "S=1 dq")
+    _close(r["dk"], np.zeros((1, 5)), 0.0, "S=1 dk")
+    _close(r["dv"], do, 1e-15, "S=1 dv")
+
+    S, hd = 9, 4
+    k, v, do = (_rand(rng, S, hd) for _ in range(3))
+    r = head(np.zeros((S, hd)), k, v, do, 0.5, True)
+    means = np.cumsum(v, axis=0) / np.arange(1, S + 1)[:, None]
+    _close(r["out"], means, 1e-14, "Q=0 out")
+    _close(r["lse"], np.log(np.arange(1, S + 1)), 1e-14, "Q=0 lse")
+
+    S = 6
+    qv = [0.3, -1.2, 0.8, 2.0, -0.4, 1.1]
+    kv = [1.5, 0.2, -0.7, 0.9, 0.4, -1.3]
+    vv = [0.5, -2.0, 1.0, 3.0, -0.5, 0.25]
+    scale = 0.9
+    r = head(np.array(qv)[:, None], np.array(kv)[:, None], np.array(vv)[:, None], None, scale, True)
+    for i in range(S):
+        logits = [scale * qv[i] * kv[j] for j in range(i + 1)]
+        m = max(logits)
+        w = [math.exp(x - m) for x in logits]
+        z = sum(w)
+        o = sum(wj * vv[j] for j, wj in enumerate(w)) / z
+        if abs(r["out"][i, 0] - o) > 1e-14 or abs(r["lse"][i] - (m + math.log(z))) > 1e-14:
+            raise AssertionError(f"hd=1 row {i}: oracle ({r['out'][i, 0]}, {r['lse'][i]}) vs ({o}, {m + math.log(z)})")
+
+
+def pin_finite_differences(head, cases=((5, 3, 1, True), (8, 4, 2, True), (6, 2, 3, False), (3, 5, 4, True)),
+                           h=1e-6, rtol=2e-7):
+    """Central differences in fp64 of f = sum(dO o O) with respect to Q, K, V."""
+    for S, hd, seed, causal in cases:
+        rng = np.random.default_rng(100 + seed)
+        x = {n: _rand(rng, S, hd) for n in ("q", "k", "v")}
+        do = _rand(rng, S, hd)
+        scale = 1.0 / math.sqrt(hd)
+        r = head(x["q"], x["k"], x["v"], do, scale, causal)
+
+        def f(**kw):
+            a = dict(x)
+            a.update(kw)
+            return float(np.sum(do * head(a["q"], a["k"], a["v"], None, scale, causal)["out"]))
+
+        for n, gname in (("q", "dq"), ("k", "dk"), ("v", "dv")):
+            g = np.zeros((S, hd))
+            for i in range(S):
+                for d in range(hd):
+                    xp = x[n].copy()
+                    xm = x[n].copy()
+                    xp[i, d] += h
+                    xm[i, d] -= h
+                    g[i, d] = (f(**{n: xp}) - f(**{n: xm})) / (2 * h)
+            tol = rtol * max(1.0, float(np.max(np.abs(g))))
+            _close(r[gname], g, tol, f"FD {gname} S={S} hd={hd} causal={causal}")
+
+
+ALL_PINS = (pin_hand_2x2, pin_row_identities, pin_dense_library, pin_special_cases, pin_finite_differences)
