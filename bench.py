@@ -1,0 +1,308 @@
+#!/usr/bin/env python3
+"""Benchmark: causal flash-attention forward + backward on one GB300.
+
+One step = one pass of the whole hot path over one batch: the forward
+(xfa_fwd) and the three backward stages (D pre-pass, backward kernel, dQ
+conversion) on the S=8192, bh=32, hd=128 bf16 workload with inputs resident
+in HBM.  Each launch is bracketed by CUDA events on the launching stream.
+The inputs (4 x 64 MiB) are larger than L2 (129 MB); no extra flush.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the CPU oracle (fp64, all host cores) on a bounded
+sample of the same workload.  Prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bwd_xfa_fwd_gb300 import inputs  # noqa: E402
+
+METRIC = "causal attn fwd / bwd TFLOP/s at 1 GB300 and fraction of bf16 tensor peak"
+WORKLOAD_ID = 5
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
+        os.environ.get("LOCAL_RANK", "0"))
+
+
+def workload_config(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "hd": w.hd, "dtype": w.dtype,
+            "scale": w.scale, "causal": True, "layout": "[bh,S,hd] row-major",
+            "l2": "inputs (4 x 64 MiB bf16) larger than L2 (129 MB); no flush"}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.result = self._collect()
+
+    def _collect(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip() == "Active"})
+        loaded = [s for s in sm if smax and s > 0.5 * max(smax)] or sm
+        return {"sm_mhz": float(np.median(loaded)) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows)}
+
+
+def make_device_inputs(w, torch):
+    x = inputs.workload_inputs(w)
+    dev = {}
+    for n in ("q", "k", "v", "dout"):
+        bits = torch.from_numpy(np.ascontiguousarray(x[n].stored).view(np.int16))
+        dev[n] = bits.view(torch.bfloat16).cuda()
+    return x, dev
+
+
+def cpu_baseline_leg(w, heads=(0, 1)):
+    """The oracle as it stands, on all host cores, on a bounded sample: the
+    forward + backward of ``heads`` of the full-size workload."""
+    import oracle
+    x = inputs.workload_inputs(w, bh=max(heads) + 1)
+    t0 = time.perf_counter()
+    oracle.attention(x["q"].exact, x["k"].exact, x["v"].exact, x["dout"].exact, w.scale, heads=list(heads))
+    dt = time.perf_counter() - t0
+    flops = (w.fwd_flops() + w.bwd_flops()) * len(heads) / w.bh
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"fwd+bwd of heads {list(heads)} of {w.name} (S={w.S}, hd={w.hd}), fp64, "
+                      f"{dt:.1f} s; FLOPs counted by the causal convention", "seconds": dt}
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    base = cpu_baseline_leg(w)
+    line = {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": 1, "warmup": 0, "ms_per_step": base["seconds"] * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), bf16-rounded)",
+            "config": workload_config(w),
+            "cpu_baseline": {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "e2e": {"value": base["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+    from bwd_xfa_fwd_gb300 import binding, build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    build.build()
+    lib = binding.load()
+    torch.cuda.init()
+    _, dev = make_device_inputs(w, torch)
+    q, k, v, do = dev["q"], dev["k"], dev["v"], dev["dout"]
+    out, lse = torch.empty_like(q), torch.empty(q.shape[:-1], device="cuda", dtype=torch.float32)
+    grads = tuple(torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(binding.workspace_bytes(w.bh, w.S, w.hd, q.dtype), device="cuda", dtype=torch.uint8)
+    stream = torch.cuda.current_stream()
+
+    stages = ("fwd", "prep", "main", "finish")
+    K = args.steps
+    ev = {s: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+          for s in stages}
+
+    def step(i=None):
+        def mark(stage, edge):
+            if i is not None:
+                ev[stage][i][edge].record(stream)
+
+        def hook(name):
+            if name == "prep":
+                mark("prep", 0)
+            elif name == "main":
+                mark("prep", 1)
+                mark("main", 0)
+            elif name == "finish":
+                mark("main", 1)
+                mark("finish", 0)
+            else:
+                mark("finish", 1)
+
+        mark("fwd", 0)
+        binding.fwd(q, k, v, w.scale, out=out, lse=lse)
+        mark("fwd", 1)
+        binding.bwd_stages(q, k, v, out, do, lse, w.scale, ws, grads, hook=hook)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if binding.status() != binding.XFA_OK:
+        raise RuntimeError("kernel status not ok after warm-up")
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(K):
+            step(i)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    if binding.status() != binding.XFA_OK:
+        raise RuntimeError("kernel status not ok after the timed region")
+    total_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    per = {s: float(np.mean([a.elapsed_time(b) for a, b in ev[s]])) for s in stages}
+    ms_step = total_ms / K
+    f_fwd, f_bwd = w.fwd_flops(), w.bwd_flops()
+    bwd_ms = per["prep"] + per["main"] + per["finish"]
+
+    # end to end through the C ABI with host buffers: pinned H2D of the step's
+    # inputs, forward + backward, D2H of O, L, dQ, dK, dV
+    host_in = {n: t.cpu().pin_memory() for n, t in dev.items()}
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (out, lse) + grads]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def e2e_step():
+        for n in ("q", "k", "v", "dout"):
+            dev[n].copy_(host_in[n], non_blocking=True)
+        binding.fwd(q, k, v, w.scale, out=out, lse=lse)
+        binding.bwd(q, k, v, out, do, lse, w.scale, workspace=ws, grads=grads)
+        for h, d in zip(host_out, (out, lse) + grads):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    ke = max(3, K // 4)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(ke):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b) / ke
+    e2e_val = (f_fwd + f_bwd) * world / (e2e_ms * 1e-3) / 1e12
+
+    pk, pk_kind = peaks()
+    peak_tc = float(pk["bf16_tflops"])
+    main_tflops = f_bwd / (per["main"] * 1e-3) / 1e12
+    prep_bytes = w.bh * w.S * (2 * w.hd * 2 + 4 + 4 + 4 + 4 * w.hd)
+    line = {
+        "metric": METRIC,
+        "value": (f_fwd + f_bwd) * world / (ms_step * 1e-3) / 1e12,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), bf16-rounded; recipe in bwd_xfa_fwd_gb300/inputs.py)",
+        "config": workload_config(w),
+        "fwd_tflops": f_fwd / (per["fwd"] * 1e-3) / 1e12,
+        "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
+        "fwd_frac_of_peak": f_fwd / (per["fwd"] * 1e-3) / 1e12 / peak_tc,
+        "bwd_frac_of_peak": f_bwd / (bwd_ms * 1e-3) / 1e12 / peak_tc,
+        "peak_bf16_tflops": peak_tc,
+        "peak_kind": f"{pk_kind} burst bf16 dense (cuBLAS)",
+        "stage_ms": per,
+        "roofline": {"kernel": "tc_bwd_kernel<128> (xfa_bwd_main)", "bound": "tensor", "achieved": main_tflops,
+                     "peak": peak_tc, "unit": "TFLOP/s", "frac": main_tflops / peak_tc, "traffic": None,
+                     "peak_source": f"{pk_kind} bf16_tflops"},
+        "roofline_fwd": {"kernel": "tc_fwd_kernel<128> (xfa_fwd)", "bound": "tensor",
+                         "achieved": f_fwd / (per["fwd"] * 1e-3) / 1e12, "peak": peak_tc, "unit": "TFLOP/s",
+                         "frac": f_fwd / (per["fwd"] * 1e-3) / 1e12 / peak_tc, "traffic": None},
+        "roofline_prep": {"kernel": "rowdot_kernel (xfa_bwd_prep)", "bound": "hbm",
+                          "achieved": prep_bytes / (per["prep"] * 1e-3) / 1e9, "peak": float(pk["hbm_gbs"]),
+                          "unit": "GB/s", "frac": prep_bytes / (per["prep"] * 1e-3) / 1e9 / float(pk["hbm_gbs"]),
+                          "traffic": None},
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": 4 * K,
+        "clocks": clk.result,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        base = cpu_baseline_leg(w)
+        line["cpu_baseline"] = {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = inputs.WORKLOADS[WORKLOAD_ID]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,63 @@
+// Internal launcher interface between the C-ABI front end (xfa_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cuda_runtime.h>
+
+#include "xfa.h"
+
+namespace xfa {
+
+struct FwdParams {
+    const void *q, *k, *v;
+    void *out;
+    float *lse;
+    int bh, S, hd;
+    float scale;
+    int dtype;
+    int *status;   // device status word
+};
+
+struct BwdParams {
+    const void *q, *k, *v, *out, *dout;
+    const float *lse;
+    void *dq, *dk, *dv;
+    int bh, S, hd;
+    float scale;
+    int dtype;
+    // workspace views
+    float *D;       // [bh][S_pad]  D_i = dO_i . O_i (0 on padded rows)
+    float *Lg;      // [bh][S_pad]  L_i * log2(e) (+inf on padded rows)
+    float *dq_acc;  // [bh][S][hd]  fp32 dQ accumulator (== dq when dtype is fp32)
+    int S_pad;
+    int *status;
+};
+
+// Rows of D / Lg are padded to a multiple of this.
+constexpr int kRowPad = 128;
+
+// SIMT (FFMA) family: any dtype, hd in {32, 64, 128}.
+cudaError_t launch_simt_fwd(const FwdParams &p, cudaStream_t st);
+cudaError_t launch_simt_bwd(const BwdParams &p, cudaStream_t st);
+
+// Backward pre-pass: D = rowdot(dO, O), Lg = lse * log2(e), padded rows filled.
+cudaError_t launch_bwd_prep(const BwdParams &p, cudaStream_t st);
+// Plain rowdot into an unpadded [bh][S] array.
+cudaError_t launch_rowdot(const void *out, const void *dout, float *d, int bh, int S, int hd, int dtype,
+                          cudaStream_t st);
+// dq (dtype) = dq_acc (fp32), n elements.
+cudaError_t launch_convert_dq(const float *acc, void *dq, size_t n, int dtype, cudaStream_t st);
+// dst += src, n elements of dtype.
+cudaError_t launch_accumulate(void *dst, const void *src, size_t n, int dtype, cudaStream_t st);
+// A kernel waiting on a barrier nothing arrives on, for at most timeout_us.
+cudaError_t launch_selftest_timeout(unsigned timeout_us, int *status, cudaStream_t st);
+
+// tcgen05 family: bf16, hd in {64, 128}.  Return an XFA_* code.
+int launch_tc_fwd(const FwdParams &p, cudaStream_t st);
+int launch_tc_bwd(const BwdParams &p, cudaStream_t st);
+
+// Encodes the TMA descriptors; resolved once from the driver (xfa_api.cu).
+int encode_tmap_bf16_3d(void *tmap, const void *base, int hd, int S, int bh, int box_rows);
+
+}  // namespace xfa

@@ -1,0 +1,438 @@
+// Flash-attention backward on the sm_103a tensor cores (bf16 in, fp32 accumulate).
+//
+// Method: "xtrain docs/13-flash-attention.md", section "什么是 flash-attention"
+// (recompute s_ij = scale Q_i.K_j and p_ij = exp(s_ij - L_i), dp_ij = dO_i.V_j,
+// ds_ij = p_ij (dp_ij - D_i) scale, then dQ_i += ds_ij K_j, dK_j += ds_ij Q_i,
+// dV_j += p_ij dO_i) with D_i = dO_i.O_i from the pre-pass (design decision ③).
+//
+// GB300 design: the key-block-owned backward that the page names as its
+// follow-up, on tcgen05:
+//   * a CTA owns 128 keys of one head; K_j and V_j are loaded once by TMA and
+//     dK_j, dV_j accumulate in TMEM (128 lanes = keys, hd fp32 columns each)
+//     over every 64-row query tile at or below the diagonal;
+//   * warp 8 streams Q_i, dO_i (TMA, 128-byte swizzle) with L_i*log2(e) and
+//     D_i (bulk copies) through a ring;
+//   * warp 9 (one thread) issues, per query tile:
+//       S^T  = K_j Q_i^T            (M=128 keys, N=64 rows, K=hd)  -> TMEM, double buffered
+//       dP^T = V_j dO_i^T           (M=128, N=64, K=hd)            -> TMEM
+//       dV  += P^T dO_i             (A = P^T bf16 in TMEM, B = dO_i MN-major)
+//       dK  += dS^T Q_i             (A = dS^T in smem, B = Q_i MN-major)
+//       dQ^T = K_j^T dS^T           (M=hd, N=64, K=128 keys)       -> TMEM
+//   * warps 0-3 (thread = key) turn S^T, dP^T into P^T (bf16, back into the
+//     S^T columns) and dS^T (bf16, swizzled smem);
+//   * warps 4-7 (thread = hd index) read dQ^T and add it into the fp32 dQ
+//     accumulator in global memory with coalesced reductions (32 consecutive
+//     floats per warp instruction); a conversion kernel writes dQ afterwards.
+// TMEM map (512 columns): dK [0,hd) dV [hd,2hd) S^T x2 [2hd,2hd+128)
+//                         dP^T [2hd+128,2hd+192) dQ^T [2hd+192,2hd+256).
+// For hd = 64 the dQ^T MMA still runs with M = 128; lanes 64-127 hold
+// products of V and are never read.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace xfa {
+namespace {
+
+constexpr int BN = 128;       // keys per CTA (MMA M)
+constexpr int BM = 64;        // query rows per tile (MMA N of S^T / dP^T)
+constexpr int NSQ = 2;        // query-tile ring depth
+constexpr int kThreads = 320;
+constexpr int kWarpTma = 8, kWarpMma = 9;
+
+template <int HD>
+struct Cfg {
+    static constexpr int SUB = HD / 64;
+    static constexpr int KV_SUB = BN * 128;             // 128 rows x 128 B
+    static constexpr int Q_SUB = BM * 128;              // 64 rows x 128 B
+    static constexpr int KV_BYTES = BN * HD * 2;
+    static constexpr int Q_BYTES = BM * HD * 2;
+    static constexpr int DS_BYTES = BN * BM * 2;        // dS^T: 128 keys x 64 rows bf16 = 128 B rows
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = KV_BYTES;
+    static constexpr int OFF_Q = 2 * KV_BYTES;
+    static constexpr int OFF_DO = OFF_Q + NSQ * Q_BYTES;
+    static constexpr int OFF_DS = OFF_DO + NSQ * Q_BYTES;
+    static constexpr int OFF_LD = OFF_DS + 2 * DS_BYTES;  // per stage: Lg[64], D[64]
+    static constexpr int OFF_BAR = OFF_LD + NSQ * 2 * BM * 4;
+    static constexpr int SMEM = OFF_BAR + 512 + 1024;
+    static constexpr uint32_t COL_DK = 0, COL_DV = HD, COL_S = 2 * HD, COL_DP = 2 * HD + 128,
+                              COL_DQ = 2 * HD + 192;
+    static constexpr uint32_t TMEM_COLS = 512;
+};
+
+struct Bars {
+    uint64_t kv_full;
+    uint64_t q_full[NSQ], q_empty[NSQ];
+    uint64_t s_full[2], p_full[2], ds_full[2], ds_empty[2];
+    uint64_t dp_full, dq_full, dq_empty, done, drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+__device__ __forceinline__ void fail(Bars *b, int *status)
+{
+    b->abort = 1;
+    record_status(status, XFA_ERR_TIMEOUT);
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, Bars *b, int *status)
+{
+    bool ok = mbar_wait(bar, parity, &b->abort);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok && (threadIdx.x & 31) == 0) fail(b, status);
+    return ok;
+}
+
+// C[M=128, N=64] = A[128 rows x hd] * B[64 rows x hd]^T, both K-major (hd contiguous).
+template <int HD>
+__device__ __forceinline__ void issue_rows_dot(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem)
+{
+    constexpr uint32_t idesc = idesc_bf16(BN, BM, false, false);
+#pragma unroll
+    for (int ks = 0; ks < HD / 16; ++ks) {
+        const uint32_t k_off = (ks % 4) * 32;
+        mma_ss(d_tmem, sdesc_sw128(a_smem + (ks / 4) * Cfg<HD>::KV_SUB + k_off, 16, 1024),
+               sdesc_sw128(b_smem + (ks / 4) * Cfg<HD>::Q_SUB + k_off, 16, 1024), idesc, ks > 0);
+    }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const float *__restrict__ Lg, const float *__restrict__ Dg, float *__restrict__ dq_acc,
+                  __nv_bfloat16 *__restrict__ dK, __nv_bfloat16 *__restrict__ dV, int bh, int S, int S_pad,
+                  float scale, float scale_log2, int *status)
+{
+    using C = Cfg<HD>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Bars *bars = reinterpret_cast<Bars *>(smem + C::OFF_BAR);
+    float *ld_s = reinterpret_cast<float *>(smem + C::OFF_LD);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    const int jt = (int)(blockIdx.x / bh);        // key tile: low tiles have the most work, go first
+    const int head = (int)(blockIdx.x % bh);
+    const int j0 = jt * BN;
+    const int nq_total = (S + BM - 1) / BM;
+    const int it0 = (j0 / BM);                    // first query tile at or below the diagonal
+    const int n = nq_total - it0;                 // >= 1
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->kv_full, 1);
+        for (int s = 0; s < NSQ; ++s) {
+            mbar_init(&bars->q_full[s], 1);
+            mbar_init(&bars->q_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->s_full[b], 1);
+            mbar_init(&bars->p_full[b], 128);
+            mbar_init(&bars->ds_full[b], 128);
+            mbar_init(&bars->ds_empty[b], 1);
+        }
+        mbar_init(&bars->dp_full, 1);
+        mbar_init(&bars->dq_full, 1);
+        mbar_init(&bars->dq_empty, HD);
+        mbar_init(&bars->done, 1);
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == kWarpTma) {
+        if (lane == 0) {
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+            prefetch_tensormap(&tm_q);
+            prefetch_tensormap(&tm_do);
+            mbar_arrive_expect_tx(&bars->kv_full, 2 * C::KV_BYTES);
+            for (int s = 0; s < C::SUB; ++s) {
+                tma_load_3d(smem + C::OFF_K + s * C::KV_SUB, &tm_k, &bars->kv_full, s * 64, j0, head);
+                tma_load_3d(smem + C::OFF_V + s * C::KV_SUB, &tm_v, &bars->kv_full, s * 64, j0, head);
+            }
+            int issued[NSQ] = {0, 0};
+            for (int it = 0; it < n; ++it) {
+                const int st = it % NSQ;
+                if (it >= NSQ && !mbar_wait(&bars->q_empty[st], ((it / NSQ) + 1) & 1, &bars->abort)) {
+                    fail(bars, status);
+                    break;
+                }
+                const int i0 = (it0 + it) * BM;
+                mbar_arrive_expect_tx(&bars->q_full[st], 2 * C::Q_BYTES + 2 * BM * 4);
+                for (int s = 0; s < C::SUB; ++s) {
+                    tma_load_3d(smem + C::OFF_Q + st * C::Q_BYTES + s * C::Q_SUB, &tm_q, &bars->q_full[st], s * 64,
+                                i0, head);
+                    tma_load_3d(smem + C::OFF_DO + st * C::Q_BYTES + s * C::Q_SUB, &tm_do, &bars->q_full[st],
+                                s * 64, i0, head);
+                }
+                float *ld = ld_s + st * 2 * BM;
+                bulk_load(ld, Lg + (size_t)head * S_pad + i0, BM * 4, &bars->q_full[st]);
+                bulk_load(ld + BM, Dg + (size_t)head * S_pad + i0, BM * 4, &bars->q_full[st]);
+                issued[st] = it + 1;
+            }
+            mbar_wait(&bars->kv_full, 0, nullptr);
+            for (int st = 0; st < NSQ; ++st)
+                if (issued[st]) mbar_wait(&bars->q_full[st], ((issued[st] - 1) / NSQ) & 1, nullptr);
+        }
+    } else if (warp == kWarpMma) {
+        if (lane == 0) {
+            const uint32_t k_s = smem_u32(smem + C::OFF_K), v_s = smem_u32(smem + C::OFF_V);
+            const uint32_t q_s = smem_u32(smem + C::OFF_Q), do_s = smem_u32(smem + C::OFF_DO);
+            const uint32_t ds_s = smem_u32(smem + C::OFF_DS);
+            constexpr uint32_t idesc_acc = idesc_bf16(BN, HD, false, true);    // dV, dK: B MN-major
+            constexpr uint32_t idesc_dq = idesc_bf16(128, BM, true, true);     // dQ^T: A, B MN-major
+            bool ok = mbar_wait(&bars->kv_full, 0, &bars->abort) && mbar_wait(&bars->q_full[0], 0, &bars->abort);
+            if (ok) {
+                tc_fence_after_sync();
+                issue_rows_dot<HD>(tmem + C::COL_S, k_s, q_s);
+                tc_commit(&bars->s_full[0]);
+                issue_rows_dot<HD>(tmem + C::COL_DP, v_s, do_s);
+                tc_commit(&bars->dp_full);
+            }
+            for (int it = 0; ok && it < n; ++it) {
+                const int b = it & 1, st = it % NSQ;
+                const uint32_t ph2 = (it >> 1) & 1;
+                const uint32_t qs = q_s + st * C::Q_BYTES, dos = do_s + st * C::Q_BYTES;
+                const uint32_t dsb = ds_s + b * C::DS_BYTES;
+                const int nx = it + 1, stn = nx % NSQ;
+                if (nx < n) {   // S^T of the next tile into the other buffer (its P was consumed in order)
+                    if (!(ok = mbar_wait(&bars->q_full[stn], (nx / NSQ) & 1, &bars->abort))) break;
+                    tc_fence_after_sync();
+                    issue_rows_dot<HD>(tmem + C::COL_S + 64 * (nx & 1), k_s, q_s + stn * C::Q_BYTES);
+                    tc_commit(&bars->s_full[nx & 1]);
+                }
+                // dV += P^T dO_i  (P^T: bf16 in the S^T columns of buffer b)
+                if (!(ok = mbar_wait(&bars->p_full[b], ph2, &bars->abort))) break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < BM / 16; ++ks)
+                    mma_ts(tmem + C::COL_DV, tmem + C::COL_S + 64 * b + ks * 8,
+                           sdesc_sw128(dos + ks * 2048, C::Q_SUB, 1024), idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
+                // dS^T is in smem and dP^T has been read: next dP^T first, then dK and dQ^T
+                if (!(ok = mbar_wait(&bars->ds_full[b], ph2, &bars->abort))) break;
+                tc_fence_after_sync();
+                if (nx < n) {
+                    issue_rows_dot<HD>(tmem + C::COL_DP, v_s, do_s + stn * C::Q_BYTES);
+                    tc_commit(&bars->dp_full);
+                }
+#pragma unroll
+                for (int ks = 0; ks < BM / 16; ++ks)
+                    mma_ss(tmem + C::COL_DK, sdesc_sw128(dsb + ks * 32, 16, 1024),
+                           sdesc_sw128(qs + ks * 2048, C::Q_SUB, 1024), idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
+                tc_commit(&bars->q_empty[st]);
+                if (it > 0 && !(ok = mbar_wait(&bars->dq_empty, (it - 1) & 1, &bars->abort))) break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < BN / 16; ++ks)
+                    mma_ss(tmem + C::COL_DQ, sdesc_sw128(k_s + ks * 2048, C::KV_SUB, 1024),
+                           sdesc_sw128(dsb + ks * 2048, C::DS_BYTES, 1024), idesc_dq, ks > 0 ? 1u : 0u);
+                tc_commit(&bars->dq_full);
+                tc_commit(&bars->ds_empty[b]);
+            }
+            if (ok) tc_commit(&bars->done);
+            else fail(bars, status);
+            tc_commit(&bars->drain);
+            mbar_wait(&bars->drain, 0, nullptr);
+        }
+    } else if (warp < 4) {
+        // thread = key row r of this CTA (TMEM lane)
+        const int r = warp * 32 + lane;
+        const int key = j0 + r;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        bool ok = true;
+        for (int it = 0; it < n; ++it) {
+            const int b = it & 1, st = it % NSQ;
+            const uint32_t ph2 = (it >> 1) & 1;
+            const int i0 = (it0 + it) * BM;
+            const float *Ls = ld_s + st * 2 * BM;
+            const float *Ds = Ls + BM;
+            if (!(ok = warp_wait(&bars->s_full[b], ph2, bars, status))) break;
+            tc_fence_after_sync();
+            uint32_t sr[64];
+            tmem_ld32(tmem + lane_off + C::COL_S + 64 * b, sr);
+            tmem_ld32(tmem + lane_off + C::COL_S + 64 * b + 32, sr + 32);
+            tmem_wait_ld();
+            reg_fence32(sr);
+            reg_fence32(sr + 32);
+            float p[64];
+            const bool diag = key > i0;   // some (key > row) pairs in this tile
+#pragma unroll
+            for (int c = 0; c < 64; c += 4) {
+                const float4 l4 = *reinterpret_cast<const float4 *>(Ls + c);
+                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float v = ex2_approx(__uint_as_float(sr[c + e]) * scale_log2 - lv[e]);
+                    if (diag && key > i0 + c + e) v = 0.0f;
+                    p[c + e] = v;
+                }
+            }
+            {
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
+                tmem_st32(tmem + lane_off + C::COL_S + 64 * b, pk);
+                tmem_wait_st();
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&bars->p_full[b]);
+
+            if (!(ok = warp_wait(&bars->dp_full, it & 1, bars, status))) break;
+            tc_fence_after_sync();
+            if (it >= 2 && !(ok = warp_wait(&bars->ds_empty[b], ph2 ^ 1, bars, status))) break;
+            uint8_t *dsrow = smem + C::OFF_DS + b * C::DS_BYTES + r * 128;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t dp[32];
+                tmem_ld32(tmem + lane_off + C::COL_DP + 32 * h, dp);
+                tmem_wait_ld();
+                reg_fence32(dp);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int c = 32 * h + 2 * e;
+                    const float d0 = p[c] * (__uint_as_float(dp[2 * e]) - Ds[c]) * scale;
+                    const float d1 = p[c + 1] * (__uint_as_float(dp[2 * e + 1]) - Ds[c + 1]) * scale;
+                    pk[e] = pack_bf16x2(d0, d1);
+                }
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int chunk = 4 * h + v;                   // 16-byte chunk of the 128-byte row
+                    uint4 w;
+                    w.x = pk[4 * v + 0];
+                    w.y = pk[4 * v + 1];
+                    w.z = pk[4 * v + 2];
+                    w.w = pk[4 * v + 3];
+                    *reinterpret_cast<uint4 *>(dsrow + ((chunk ^ (r & 7)) << 4)) = w;
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            mbar_arrive(&bars->ds_full[b]);
+        }
+        // epilogue: dV rows
+        if (ok && warp_wait(&bars->done, 0, bars, status)) {
+            tc_fence_after_sync();
+            __nv_bfloat16 *dst = dV + ((size_t)head * S + key) * HD;
+#pragma unroll 1
+            for (int c = 0; c < HD; c += 32) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + C::COL_DV + c, o);
+                tmem_wait_ld();
+                reg_fence32(o);
+                if (key < S) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]), __uint_as_float(o[8 * v + 1]));
+                        w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]), __uint_as_float(o[8 * v + 3]));
+                        w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]), __uint_as_float(o[8 * v + 5]));
+                        w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]), __uint_as_float(o[8 * v + 7]));
+                        reinterpret_cast<uint4 *>(dst + c)[v] = w;
+                    }
+                }
+            }
+        }
+    } else if (warp < 8) {
+        // dQ readout: thread = hd index d (TMEM lane of dQ^T)
+        const int wq = warp - 4;
+        const int d = wq * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        bool ok = true;
+        if (d < HD) {
+            for (int it = 0; it < n; ++it) {
+                if (!(ok = warp_wait(&bars->dq_full, it & 1, bars, status))) break;
+                tc_fence_after_sync();
+                uint32_t g[64];
+                tmem_ld32(tmem + lane_off + C::COL_DQ, g);
+                tmem_ld32(tmem + lane_off + C::COL_DQ + 32, g + 32);
+                tmem_wait_ld();
+                reg_fence32(g);
+                reg_fence32(g + 32);
+                tc_fence_before_sync();
+                mbar_arrive(&bars->dq_empty);
+                const int i0 = (it0 + it) * BM;
+                float *dst = dq_acc + ((size_t)head * S + i0) * HD + d;
+                const int rows = min(BM, S - i0);
+#pragma unroll 8
+                for (int c = 0; c < BM; ++c)
+                    if (c < rows) atomicAdd(dst + (size_t)c * HD, __uint_as_float(g[c]));
+            }
+        }
+        // epilogue: dK rows (same TMEM lanes as warps 0-3: thread = key)
+        const int key = j0 + wq * 32 + lane;
+        if (ok && warp_wait(&bars->done, 0, bars, status)) {
+            tc_fence_after_sync();
+            __nv_bfloat16 *dst = dK + ((size_t)head * S + key) * HD;
+#pragma unroll 1
+            for (int c = 0; c < HD; c += 32) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + C::COL_DK + c, o);
+                tmem_wait_ld();
+                reg_fence32(o);
+                if (key < S) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]), __uint_as_float(o[8 * v + 1]));
+                        w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]), __uint_as_float(o[8 * v + 3]));
+                        w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]), __uint_as_float(o[8 * v + 5]));
+                        w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]), __uint_as_float(o[8 * v + 7]));
+                        reinterpret_cast<uint4 *>(dst + c)[v] = w;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int HD>
+int run(const BwdParams &p, cudaStream_t st)
+{
+    alignas(64) CUtensorMap tk, tv, tq, tdo;
+    int rc = encode_tmap_bf16_3d(&tk, p.k, HD, p.S, p.bh, BN);
+    if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tv, p.v, HD, p.S, p.bh, BN);
+    if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tq, p.q, HD, p.S, p.bh, BM);
+    if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tdo, p.dout, HD, p.S, p.bh, BM);
+    if (rc != XFA_OK) return rc;
+    auto kern = tc_bwd_kernel<HD>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<HD>::SMEM);
+    if (e != cudaSuccess) return XFA_ERR_CUDA_BASE + (int)e;
+    const int nkt = (p.S + BN - 1) / BN;
+    const unsigned grid = (unsigned)(nkt * p.bh);
+    kern<<<grid, kThreads, Cfg<HD>::SMEM, st>>>(tk, tv, tq, tdo, p.Lg, p.D, p.dq_acc, (__nv_bfloat16 *)p.dk,
+                                                 (__nv_bfloat16 *)p.dv, p.bh, p.S, p.S_pad, p.scale,
+                                                 p.scale * 1.4426950408889634f, p.status);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? XFA_OK : XFA_ERR_CUDA_BASE + (int)e;
+}
+
+}  // namespace
+
+int launch_tc_bwd(const BwdParams &p, cudaStream_t st)
+{
+    if (p.dtype != XFA_BF16) return XFA_ERR_UNSUPPORTED;
+    if (p.hd == 128) return run<128>(p, st);
+    if (p.hd == 64) return run<64>(p, st);
+    return XFA_ERR_UNSUPPORTED;
+}
+
+}  // namespace xfa

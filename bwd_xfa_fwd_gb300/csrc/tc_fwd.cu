@@ -1,0 +1,373 @@
+// Flash-attention forward on the sm_103a tensor cores (bf16 in, fp32 accumulate).
+//
+// Method: "xtrain docs/13-flash-attention.md", section "什么是 flash-attention":
+// for each query row, scan the key/value tiles at or below the diagonal with
+// the online softmax (running max m, running sum l, accumulator rescaled by
+// exp(m_old - m_new)), finish with out = acc / l and L = m + ln l; tiles wholly
+// above the diagonal are never touched.
+//
+// GB300 design (replaces the page's one-block-per-row SIMT kernel):
+//   * a CTA owns 256 query rows of one head as two 128-row tiles (t = 0, 1);
+//   * warp 8 streams K and V tiles (128 keys x hd) through a TMA ring with
+//     128-byte swizzle; Q tiles are loaded once;
+//   * warp 9 (one thread) issues tcgen05.mma: S_t = Q_t K^T into TMEM
+//     (128 lanes x 128 fp32 columns) and O_t += P_t V with P_t read straight
+//     from TMEM (bf16, packed into the first 64 columns of S_t);
+//   * warps 0-3 and 4-7 are the softmax groups of tiles 0 and 1: thread = row,
+//     tcgen05.ld of the S row, scaled exp2, row max / sum in registers, P
+//     written back with tcgen05.st.  While one group works on its S tile the
+//     tensor core runs the other tile's MMAs.
+//   * The O rescale is lazy: the reference maximum only moves when a row max
+//     exceeds it by more than 2^8 (in exp2 units), so P <= 256 and fp32
+//     accumulation is unaffected; when it moves, the warp rescales its O rows
+//     in TMEM after the previous P.V has completed (guaranteed by the S-ready
+//     commit, which tracks every earlier MMA).
+// TMEM map (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+hd) O1 [256+hd, 256+2hd).
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace xfa {
+namespace {
+
+constexpr int BM = 128;               // query rows per tile (MMA M)
+constexpr int BN = 128;               // keys per tile (MMA N of S, K of P.V)
+constexpr int kThreads = 320;         // 10 warps
+constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+template <int HD>
+struct Cfg {
+    static constexpr int SUB = HD / 64;                 // 128-byte column blocks per row
+    static constexpr int SUB_BYTES = 128 * 128;         // 128 rows x 128 B
+    static constexpr int TILE_BYTES = BM * HD * 2;      // BM == BN
+    static constexpr int NS = HD == 128 ? 2 : 3;        // K/V ring depth
+    static constexpr int OFF_Q0 = 0;
+    static constexpr int OFF_Q1 = TILE_BYTES;
+    static constexpr int OFF_K = 2 * TILE_BYTES;
+    static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
+    static constexpr int OFF_BAR = OFF_V + NS * TILE_BYTES;
+    static constexpr int SMEM = OFF_BAR + 512 + 1024;   // barriers + alignment slack
+    // TMEM columns of S_t and O_t
+    static __device__ __forceinline__ uint32_t col_s(int t) { return 128u * (uint32_t)t; }
+    static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + (uint32_t)(HD * t); }
+};
+
+struct Bars {
+    uint64_t q_full;
+    uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
+    uint64_t s_full[2];   // S_t ready in TMEM (tensor-core commit)
+    uint64_t p_full[2];   // P_t written to TMEM (128 softmax threads)
+    uint64_t o_full[2];   // O_t complete (commit after the last P.V)
+    uint64_t drain;       // MMA drain at teardown
+    uint32_t tmem_base;
+    int abort;
+};
+
+__device__ __forceinline__ void fail(Bars *b, int *status)
+{
+    b->abort = 1;
+    record_status(status, XFA_ERR_TIMEOUT);
+}
+
+// All lanes wait; the outcome is made warp-uniform so warp-collective
+// tcgen05 instructions after it are never reached by part of a warp.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, Bars *b, int *status)
+{
+    bool ok = mbar_wait(bar, parity, &b->abort);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok && (threadIdx.x & 31) == 0) fail(b, status);
+    return ok;
+}
+
+template <int HD>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem)
+{
+    constexpr uint32_t idesc = idesc_bf16(BM, BN, false, false);
+#pragma unroll
+    for (int ks = 0; ks < HD / 16; ++ks) {
+        const uint32_t off = (ks / 4) * Cfg<HD>::SUB_BYTES + (ks % 4) * 32;
+        mma_ss(d_tmem, sdesc_sw128(q_smem + off, 16, 1024), sdesc_sw128(k_smem + off, 16, 1024), idesc, ks > 0);
+    }
+}
+
+template <int HD>
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem, bool accumulate)
+{
+    constexpr uint32_t idesc = idesc_bf16(BM, HD, false, true);
+#pragma unroll
+    for (int ks = 0; ks < BN / 16; ++ks) {
+        // V is [keys][hd]: MN-major B operand; 16 keys = 2048 bytes, hd blocks of 64 are SUB_BYTES apart.
+        mma_ts(o_tmem, p_tmem + ks * 8, sdesc_sw128(v_smem + ks * 2048, Cfg<HD>::SUB_BYTES, 1024), idesc,
+               (accumulate || ks > 0) ? 1u : 0u);
+    }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ O,
+                  float *__restrict__ lse, int bh, int S, float scale_log2, int *status)
+{
+    using C = Cfg<HD>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Bars *bars = reinterpret_cast<Bars *>(smem + C::OFF_BAR);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    const int nqb = (S + 2 * BM - 1) / (2 * BM);
+    const int qb = nqb - 1 - (int)(blockIdx.x / bh);   // heaviest query blocks first
+    const int head = (int)(blockIdx.x % bh);
+    const int q0 = qb * 2 * BM;
+    const bool t1 = q0 + BM < S;
+    const int n_t[2] = {2 * qb + 1, t1 ? 2 * qb + 2 : 0};   // key tiles per query tile
+    const int nkv = t1 ? n_t[1] : n_t[0];
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->q_full, 1);
+        for (int s = 0; s < 3; ++s) {
+            mbar_init(&bars->k_full[s], 1);
+            mbar_init(&bars->k_empty[s], 1);
+            mbar_init(&bars->v_full[s], 1);
+            mbar_init(&bars->v_empty[s], 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&bars->s_full[t], 1);
+            mbar_init(&bars->p_full[t], BM);
+            mbar_init(&bars->o_full[t], 1);
+        }
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(&bars->tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == kWarpTma) {
+        if (lane == 0) {
+            prefetch_tensormap(&tm_q);
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+            int issued[3] = {0, 0, 0};
+            mbar_arrive_expect_tx(&bars->q_full, (t1 ? 2 : 1) * C::TILE_BYTES);
+            for (int s = 0; s < C::SUB; ++s) {
+                tma_load_3d(smem + C::OFF_Q0 + s * C::SUB_BYTES, &tm_q, &bars->q_full, s * 64, q0, head);
+                if (t1) tma_load_3d(smem + C::OFF_Q1 + s * C::SUB_BYTES, &tm_q, &bars->q_full, s * 64, q0 + BM, head);
+            }
+            for (int j = 0; j < nkv; ++j) {
+                const int st = j % C::NS;
+                const uint32_t ph = ((j / C::NS) + 1) & 1;   // parity of the release of the previous use
+                if (j >= C::NS && !mbar_wait(&bars->k_empty[st], ph, &bars->abort)) { fail(bars, status); break; }
+                mbar_arrive_expect_tx(&bars->k_full[st], C::TILE_BYTES);
+                for (int s = 0; s < C::SUB; ++s)
+                    tma_load_3d(smem + C::OFF_K + st * C::TILE_BYTES + s * C::SUB_BYTES, &tm_k, &bars->k_full[st],
+                                s * 64, j * BN, head);
+                if (j >= C::NS && !mbar_wait(&bars->v_empty[st], ph, &bars->abort)) {
+                    issued[st] = j + 1;   // K of round j was issued
+                    fail(bars, status);
+                    break;
+                }
+                mbar_arrive_expect_tx(&bars->v_full[st], C::TILE_BYTES);
+                for (int s = 0; s < C::SUB; ++s)
+                    tma_load_3d(smem + C::OFF_V + st * C::TILE_BYTES + s * C::SUB_BYTES, &tm_v, &bars->v_full[st],
+                                s * 64, j * BN, head);
+                issued[st] = j + 1;
+            }
+            // Never leave the CTA with copies in flight: wait for the last load of each stage.
+            mbar_wait(&bars->q_full, 0, nullptr);
+            for (int st = 0; st < C::NS; ++st) {
+                if (issued[st] == 0) continue;
+                const uint32_t ph = ((issued[st] - 1) / C::NS) & 1;
+                mbar_wait(&bars->k_full[st], ph, nullptr);
+                mbar_wait(&bars->v_full[st], ph, nullptr);
+            }
+        }
+    } else if (warp == kWarpMma) {
+        if (lane == 0) {
+            const uint32_t q_s[2] = {smem_u32(smem + C::OFF_Q0), smem_u32(smem + C::OFF_Q1)};
+            const uint32_t k_s = smem_u32(smem + C::OFF_K), v_s = smem_u32(smem + C::OFF_V);
+            bool ok = mbar_wait(&bars->q_full, 0, &bars->abort) && mbar_wait(&bars->k_full[0], 0, &bars->abort);
+            if (ok) {
+                tc_fence_after_sync();
+                for (int t = 0; t < 2; ++t) {
+                    if (n_t[t] == 0) continue;
+                    issue_qk<HD>(tmem + C::col_s(t), q_s[t], k_s);
+                    tc_commit(&bars->s_full[t]);
+                }
+                tc_commit(&bars->k_empty[0]);
+            }
+            for (int j = 0; ok && j < nkv; ++j) {
+                const int st = j % C::NS;
+                const uint32_t ph = (j / C::NS) & 1;
+                bool v_ready = false, k_next_ready = false;
+                const int jn = j + 1, stn = jn % C::NS;
+                const uint32_t phn = (jn / C::NS) & 1;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j >= n_t[t]) continue;
+                    ok = mbar_wait(&bars->p_full[t], j & 1, &bars->abort);
+                    if (ok && !v_ready) ok = v_ready = mbar_wait(&bars->v_full[st], ph, &bars->abort);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    issue_pv<HD>(tmem + C::col_o(t), tmem + C::col_s(t), v_s + st * C::TILE_BYTES, j > 0);
+                    if (j == n_t[t] - 1) tc_commit(&bars->o_full[t]);
+                    if (jn < n_t[t]) {
+                        if (!k_next_ready) ok = k_next_ready = mbar_wait(&bars->k_full[stn], phn, &bars->abort);
+                        if (!ok) break;
+                        tc_fence_after_sync();
+                        issue_qk<HD>(tmem + C::col_s(t), q_s[t], k_s + stn * C::TILE_BYTES);
+                        tc_commit(&bars->s_full[t]);
+                    }
+                }
+                if (!ok) break;
+                if (k_next_ready) tc_commit(&bars->k_empty[stn]);
+                tc_commit(&bars->v_empty[st]);
+            }
+            if (!ok) fail(bars, status);
+            tc_commit(&bars->drain);
+            mbar_wait(&bars->drain, 0, nullptr);
+        }
+    } else {
+        // softmax group of tile t; thread = query row
+        const int t = warp / 4, wq = warp % 4;
+        const int r = wq * 32 + lane;               // row within the tile == TMEM lane
+        const int row = q0 + t * BM + r;
+        const int diag = 2 * qb + t;                // key tile that holds this tile's diagonal
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off + C::col_s(t);
+        const uint32_t tO = tmem + lane_off + C::col_o(t);
+        float m = -CUDART_INF_F, l = 0.0f;
+        bool ok = true;
+        for (int j = 0; j < n_t[t]; ++j) {
+            if (!(ok = warp_wait(&bars->s_full[t], j & 1, bars, status))) break;
+            tc_fence_after_sync();
+            uint32_t sr[128];
+            tmem_ld32(tS + 0, sr + 0);
+            tmem_ld32(tS + 32, sr + 32);
+            tmem_ld32(tS + 64, sr + 64);
+            tmem_ld32(tS + 96, sr + 96);
+            tmem_wait_ld();
+            reg_fence32(sr + 0);
+            reg_fence32(sr + 32);
+            reg_fence32(sr + 64);
+            reg_fence32(sr + 96);
+            float x[128];
+#pragma unroll
+            for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]) * scale_log2;
+            if (j == diag) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (c > r) x[c] = -CUDART_INF_F;
+            }
+            float mx = x[0];
+#pragma unroll
+            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+            const float m_new = fmaxf(m, mx);
+            const bool need = m_new > m + kRescaleThreshold;
+            if (__any_sync(0xffffffffu, need)) {
+                const float alpha = ex2_approx(m - m_new);   // 0 on the first tile
+                l *= alpha;
+                if (j > 0) {
+#pragma unroll 1
+                    for (int c = 0; c < HD; c += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c, o);
+                        tmem_wait_ld();
+                        reg_fence32(o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(tO + c, o);
+                    }
+                    tmem_wait_st();
+                }
+                m = m_new;
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float p0 = ex2_approx(x[64 * h + 2 * e] - m);
+                    const float p1 = ex2_approx(x[64 * h + 2 * e + 1] - m);
+                    l += p0 + p1;
+                    pk[e] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(tS + 32 * h, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before_sync();
+            mbar_arrive(&bars->p_full[t]);
+        }
+        if (ok && n_t[t] > 0 && warp_wait(&bars->o_full[t], 0, bars, status)) {
+            tc_fence_after_sync();
+            const float inv_l = 1.0f / l;
+            __nv_bfloat16 *orow = O + ((size_t)head * S + row) * HD;
+#pragma unroll 1
+            for (int c = 0; c < HD; c += 32) {
+                uint32_t o[32];
+                tmem_ld32(tO + c, o);
+                tmem_wait_ld();
+                reg_fence32(o);
+                if (row < S) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
+                        w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
+                        w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
+                        w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
+                        dst[v] = w;
+                    }
+                }
+            }
+            if (row < S) lse[(size_t)head * S + row] = (m + __log2f(l)) * kLn2;
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int HD>
+int run(const FwdParams &p, cudaStream_t st)
+{
+    alignas(64) CUtensorMap tq, tk, tv;
+    int rc = encode_tmap_bf16_3d(&tq, p.q, HD, p.S, p.bh, BM);
+    if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tk, p.k, HD, p.S, p.bh, BN);
+    if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tv, p.v, HD, p.S, p.bh, BN);
+    if (rc != XFA_OK) return rc;
+    auto kern = tc_fwd_kernel<HD>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<HD>::SMEM);
+    if (e != cudaSuccess) return XFA_ERR_CUDA_BASE + (int)e;
+    const int nqb = (p.S + 2 * BM - 1) / (2 * BM);
+    const unsigned grid = (unsigned)(nqb * p.bh);
+    kern<<<grid, kThreads, Cfg<HD>::SMEM, st>>>(tq, tk, tv, (__nv_bfloat16 *)p.out, p.lse, p.bh, p.S,
+                                                 p.scale * 1.4426950408889634f, p.status);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? XFA_OK : XFA_ERR_CUDA_BASE + (int)e;
+}
+
+}  // namespace
+
+int launch_tc_fwd(const FwdParams &p, cudaStream_t st)
+{
+    if (p.dtype != XFA_BF16) return XFA_ERR_UNSUPPORTED;
+    if (p.hd == 128) return run<128>(p, st);
+    if (p.hd == 64) return run<64>(p, st);
+    return XFA_ERR_UNSUPPORTED;
+}
+
+}  // namespace xfa

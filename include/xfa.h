@@ -1,0 +1,185 @@
+/*
+ * xfa.h -- C ABI of libxfa.so: fused causal flash-attention, forward and
+ * backward, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is causal scaled-dot-product attention as defined in
+ * "xtrain docs/13-flash-attention.md", section "什么是 flash-attention":
+ *
+ *   s_ij = scale * Q_i . K_j           for key j <= query i (j > i is masked)
+ *   P_ij = softmax_j(s_ij)             row-wise over the unmasked keys
+ *   O_i  = sum_j P_ij V_j
+ *   L_i  = m_i + ln(l_i) = ln sum_j exp(s_ij)     (natural-log logsumexp)
+ *
+ * and its gradients through the same page's flash backward
+ * (D_i = dO_i . O_i,  dS_ij = P_ij (dP_ij - D_i) scale,  dP_ij = dO_i . V_j):
+ *
+ *   dQ_i = sum_j dS_ij K_j,   dK_j = sum_i dS_ij Q_i,   dV_j = sum_i P_ij dO_i.
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors Q, K, V, O, dO, dQ, dK, dV are contiguous row-major [bh][S][hd]
+ *     arrays in device memory, element type given by `dtype` (xfa_dtype).
+ *     bh = batch * heads; every head is an independent problem.  The query
+ *     position used by the causal mask is the row index within S (the
+ *     "i % S" of the page's flattened [B*S] rows).
+ *   - lse is a contiguous [bh][S] fp32 device array (natural log).
+ *   - Pointers must be 16-byte aligned device pointers and must not alias
+ *     each other (inputs may alias inputs).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     call only enqueues work on `stream` and returns; it never synchronises,
+ *     allocates or frees memory.  The caller owns every buffer.
+ *   - Supported shapes: bh >= 1, S >= 1 (any S: ragged tails are masked),
+ *     hd in {32, 64, 128}; bh * S * hd < 2^31.  scale must be finite and > 0.
+ *   - Return value: XFA_OK, or an error code.  Argument errors are detected
+ *     on the host before anything is enqueued, and nothing is written.
+ *     A CUDA launch error is returned as XFA_ERR_CUDA_BASE + cudaError_t.
+ *     A kernel that gives up waiting on its own pipeline (see xfa_status)
+ *     leaves its outputs undefined.
+ */
+#ifndef XFA_H
+#define XFA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of Q, K, V, O, dO, dQ, dK, dV.  Arithmetic is fp32 throughout
+ * (fp32 accumulation; bf16 operands feed the tensor cores). */
+typedef enum { XFA_F32 = 0, XFA_BF16 = 1 } xfa_dtype;
+
+/* Kernel family selector for the *_impl entry points. */
+typedef enum {
+    XFA_IMPL_AUTO = 0,    /* tcgen05 tensor-core kernels where supported, else SIMT */
+    XFA_IMPL_SIMT = 1,    /* fp32 FFMA tiled kernels (every dtype and hd) */
+    XFA_IMPL_TCGEN05 = 2  /* bf16, hd in {64, 128}: TMA + tcgen05.mma + TMEM kernels */
+} xfa_impl;
+
+enum {
+    XFA_OK = 0,
+    XFA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, bad scale */
+    XFA_ERR_UNSUPPORTED = 2,  /* valid but unsupported combination (hd, dtype, impl) */
+    XFA_ERR_TIMEOUT = 3,      /* a kernel gave up waiting on its pipeline (xfa_status) */
+    XFA_ERR_WORKSPACE = 4,    /* workspace missing or smaller than xfa_bwd_workspace_bytes */
+    XFA_ERR_DEVICE = 5,       /* no usable device, or not an sm_103 device for tcgen05 */
+    XFA_ERR_CUDA_BASE = 1000  /* + cudaError_t of a failed CUDA runtime call */
+};
+
+/*
+ * Forward.  Passage: "xtrain docs/13-flash-attention.md", section
+ * "什么是 flash-attention" (online-softmax recurrence over KV tiles with running
+ * max m, running sum l and an [hd] accumulator; out = acc / l; L = m + log l;
+ * tiles wholly above the diagonal skipped) and design decision ② (only the
+ * O(N) logsumexp is kept for the backward).
+ *   q, k, v : [bh][S][hd] inputs (dtype)
+ *   out     : [bh][S][hd] output O (dtype), overwritten
+ *   lse     : [bh][S] fp32 output L (natural log), overwritten
+ */
+int xfa_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
+            int bh, int S, int hd, float scale, int dtype, void *stream);
+
+/* xfa_fwd with an explicit kernel family (xfa_impl). */
+int xfa_fwd_impl(const void *q, const void *k, const void *v, void *out, float *lse,
+                 int bh, int S, int hd, float scale, int dtype, int impl, void *stream);
+
+/*
+ * Bytes of device workspace xfa_bwd needs for this shape (a pure function of
+ * its arguments; 0 for invalid arguments).  Holds D [bh][S'] and L*log2(e)
+ * [bh][S'] fp32 (S' = S rounded up to 128) and, for bf16, an fp32 dQ
+ * accumulator [bh][S][hd].
+ */
+size_t xfa_bwd_workspace_bytes(int bh, int S, int hd, int dtype);
+
+/*
+ * Backward.  Passage: "xtrain docs/13-flash-attention.md", section
+ * "什么是 flash-attention" (recompute s_ij and p_ij = exp(s_ij - L_i) from Q, K
+ * and L; dp_ij = dO_i . V_j; ds_ij = p_ij (dp_ij - D_i) scale; dQ, dK, dV
+ * accumulation) and design decision ③ (D_i = sum_d dO_i[d] O_i[d] computed in
+ * one pass first).
+ *   q, k, v      : forward inputs (dtype)
+ *   out, lse     : forward outputs O (dtype) and L (fp32) of the same call
+ *   dout         : [bh][S][hd] upstream gradient dO (dtype)
+ *   dq, dk, dv   : [bh][S][hd] gradients (dtype), OVERWRITTEN (not accumulated;
+ *                  fan-out accumulation is the caller's, e.g. xfa_accumulate)
+ *   workspace    : device scratch of at least xfa_bwd_workspace_bytes() bytes,
+ *                  16-byte aligned; contents on entry are ignored
+ * Enqueues, in order on `stream`: the D pre-pass, the backward kernel and,
+ * for bf16, the dQ fp32 -> bf16 conversion.
+ */
+int xfa_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout,
+            const float *lse, void *dq, void *dk, void *dv,
+            int bh, int S, int hd, float scale, int dtype,
+            void *workspace, size_t workspace_bytes, void *stream);
+
+/* xfa_bwd with an explicit kernel family (xfa_impl). */
+int xfa_bwd_impl(const void *q, const void *k, const void *v, const void *out, const void *dout,
+                 const float *lse, void *dq, void *dk, void *dv,
+                 int bh, int S, int hd, float scale, int dtype,
+                 void *workspace, size_t workspace_bytes, int impl, void *stream);
+
+/*
+ * The three stages of xfa_bwd as separate calls, for callers that schedule
+ * (or time) them individually.  xfa_bwd_impl is exactly prep, main, finish
+ * in this order on one stream, with the same arguments and workspace.
+ *   prep   : D_i = dO_i . O_i and L_i * log2(e) into the workspace (padded
+ *            rows: D = 0, L = +inf), and clears the fp32 dQ accumulator (the
+ *            workspace for bf16, dq itself for fp32).
+ *   main   : the backward kernel (dK, dV written; dQ summed into the accumulator).
+ *   finish : dQ accumulator -> dq in the output dtype (nothing to do for fp32).
+ * Same argument rules and error codes as xfa_bwd.
+ */
+int xfa_bwd_prep(const void *out, const void *dout, const float *lse, void *dq, int bh, int S, int hd, int dtype,
+                 void *workspace, size_t workspace_bytes, void *stream);
+int xfa_bwd_main(const void *q, const void *k, const void *v, const void *dout, void *dq, void *dk, void *dv,
+                 int bh, int S, int hd, float scale, int dtype, void *workspace, size_t workspace_bytes, int impl,
+                 void *stream);
+int xfa_bwd_finish(void *dq, int bh, int S, int hd, int dtype, void *workspace, size_t workspace_bytes,
+                   void *stream);
+
+/*
+ * The backward's pre-pass on its own: D[b][i] = sum_d dout[b][i][d] * out[b][i][d]
+ * with fp32 accumulation.  Passage: "xtrain docs/13-flash-attention.md",
+ * design decision ③ (D_i = sum_d dO_i[d] O_i[d]).
+ *   out, dout : [bh][S][hd] (dtype);  d : [bh][S] fp32 output, overwritten.
+ */
+int xfa_rowdot(const void *out, const void *dout, float *d, int bh, int S, int hd, int dtype, void *stream);
+
+/*
+ * dst[i] += src[i] for i < n (dtype elements, fp32 arithmetic).  The tape's
+ * fan-out gradient accumulation: "xtrain docs/03-autograd-engine.md", section
+ * "梯度累加（扇出求和）" (every push_grad sums into the existing gradient).
+ * dst and src must not overlap partially.
+ */
+int xfa_accumulate(void *dst, const void *src, size_t n, int dtype, void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device status
+ * word on the current device.  Returns XFA_OK, XFA_ERR_TIMEOUT when a kernel
+ * since the last call gave up on a pipeline wait (every wait in every kernel
+ * has a time limit of about one second, after which the kernel records the
+ * timeout, drains its own in-flight copies, frees its tensor memory and
+ * exits), or XFA_ERR_CUDA_BASE + a CUDA error.
+ */
+int xfa_status(void *stream);
+
+/*
+ * Self-test of the timeout path: enqueues one single-CTA kernel that waits on
+ * a shared-memory barrier which nothing ever arrives on, with a limit of
+ * `timeout_us` microseconds (1 .. 1000000).  The kernel then records
+ * XFA_ERR_TIMEOUT in the status word and returns; read it with xfa_status.
+ * No counterpart on the pages: it exists so the timeout path can be tested
+ * without hanging a GPU.
+ */
+int xfa_selftest_timeout(unsigned timeout_us, void *stream);
+
+/* Static description of an error code. */
+const char *xfa_strerror(int code);
+
+/* ABI version (major * 100 + minor). */
+int xfa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* XFA_H */

@@ -1,0 +1,171 @@
+"""CUDA path against the CPU oracle on identical seeded inputs (GB300 only).
+
+Every call goes through the C ABI (ctypes binding).  Workloads 1-3 are compared
+in full; workloads 4-5 (S=4096 and S=8192) in the launch configuration the
+benchmark times, on sampled heads the oracle computes exactly, plus identities
+that hold for every head at any size."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from bwd_xfa_fwd_gb300 import inputs
+from tests.gpu_helpers import TOL, compare, oracle_result, run_gpu, to_device, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from bwd_xfa_fwd_gb300 import binding, build
+    build.build()
+    binding.load()
+    assert torch.cuda.is_available()
+
+
+@pytest.mark.parametrize("wid", [1, 2, 3])
+def test_workload_full(wid):
+    w = inputs.WORKLOADS[wid]
+    x = inputs.workload_inputs(w)
+    got = run_gpu(x, w.dtype, w.scale)
+    ref = oracle_result(("w", wid), x, w.scale)
+    compare(got, ref, w.dtype)
+
+
+def _identities(got, x, dtype):
+    """Exact identities of the operator, checked on every head:
+    sum_j dV_j = sum_i dO_i (rows of P sum to 1);  sum_j dK_j = 0 (rows of dS sum
+    to 0);  tr(Q^T dQ) = tr(K^T dK) (s depends on Q, K only through Q K^T)."""
+    tol = TOL[dtype]["rel"]
+    dout = x["dout"].exact
+    sv = got["dv"].sum(axis=1) - dout.sum(axis=1)
+    assert np.max(np.abs(sv)) <= tol * np.max(np.abs(got["dv"]).sum(axis=1)), "sum dV != sum dO"
+    sk = got["dk"].sum(axis=1)
+    assert np.max(np.abs(sk)) <= tol * np.max(np.abs(got["dk"]).sum(axis=1)), "sum dK != 0"
+    tq = np.einsum("bsd,bsd->b", x["q"].exact, got["dq"])
+    tk = np.einsum("bsd,bsd->b", x["k"].exact, got["dk"])
+    mag = np.einsum("bsd,bsd->b", np.abs(x["q"].exact), np.abs(got["dq"]))
+    assert np.all(np.abs(tq - tk) <= tol * mag), "tr(Q^T dQ) != tr(K^T dK)"
+
+
+@pytest.mark.parametrize("wid,heads", [(4, (0, 37, 63)), (5, (0, 31))])
+def test_workload_full_size_sampled(wid, heads):
+    w = inputs.WORKLOADS[wid]
+    x = inputs.workload_inputs(w)
+    got = run_gpu(x, w.dtype, w.scale)
+    for n in ("out", "lse", "dq", "dk", "dv"):
+        assert np.all(np.isfinite(got[n])), n
+    ref = oracle_result(("w", wid), x, w.scale, heads=list(heads))
+    compare(got, ref, w.dtype, heads=heads)
+    _identities(got, x, w.dtype)
+
+
+RAGGED = [1, 5, 64, 100, 128, 129, 255, 256, 257, 300, 511, 777]
+
+
+@pytest.mark.parametrize("S", RAGGED)
+@pytest.mark.parametrize("dtype,hd,impl", [("bf16", 128, 2), ("bf16", 64, 2), ("bf16", 32, 1), ("f32", 32, 1),
+                                           ("f32", 64, 1), ("f32", 128, 1), ("bf16", 128, 1)])
+def test_ragged_and_small(S, dtype, hd, impl):
+    bh = 3
+    scale = 1.0 / math.sqrt(hd)
+    x = inputs.draw((bh, S, hd), dtype, seed=1000 + S + hd, stds=(1.0, 1.0, 1.0, 1.0))
+    got = run_gpu(x, dtype, scale, impl=impl)
+    ref = oracle_result(("ragged", S, hd, dtype), x, scale)
+    compare(got, ref, dtype)
+
+
+@pytest.mark.parametrize("hd", [64, 128])
+def test_tcgen05_and_simt_agree_with_oracle(hd):
+    S, bh = 1024, 4
+    scale = 1.0 / math.sqrt(hd)
+    x = inputs.draw((bh, S, hd), "bf16", seed=77 + hd, stds=(2.0, 2.0, 1.0, 1.0))
+    ref = oracle_result(("both", hd), x, scale)
+    for impl in (1, 2):
+        compare(run_gpu(x, "bf16", scale, impl=impl), ref, "bf16")
+
+
+@pytest.mark.parametrize("dtype,hd", [("f32", 32), ("f32", 128), ("bf16", 64), ("bf16", 128)])
+def test_rowdot(dtype, hd):
+    from bwd_xfa_fwd_gb300 import binding
+    x = inputs.draw((5, 333, hd), dtype, seed=5, names=("q", "k"))
+    o, do = to_device(x["q"], dtype), to_device(x["k"], dtype)
+    d = to_f64(binding.rowdot(o, do))
+    ref = np.sum(x["q"].exact * x["k"].exact, axis=-1)
+    assert np.max(np.abs(d - ref)) <= 1e-5 * np.max(np.abs(ref))
+
+
+def test_outputs_do_not_write_outside_their_buffers():
+    """Canary guards around every output buffer stay untouched."""
+    from bwd_xfa_fwd_gb300 import binding
+    bh, S, hd = 2, 300, 128
+    scale = 1.0 / math.sqrt(hd)
+    x = inputs.draw((bh, S, hd), "bf16", seed=9)
+    q, k, v, do = (to_device(x[n], "bf16") for n in ("q", "k", "v", "dout"))
+    n = bh * S * hd
+    guard = 4096
+
+    def guarded(numel, dtype):
+        buf = torch.full((numel + 2 * guard,), -7.0, device="cuda", dtype=dtype)
+        return buf, buf[guard:guard + numel]
+
+    for impl in (1, 2):
+        bo, out = guarded(n, torch.bfloat16)
+        bl, lse = guarded(bh * S, torch.float32)
+        binding.fwd(q, k, v, scale, impl, out=out.view(bh, S, hd), lse=lse.view(bh, S))
+        grads = [guarded(n, torch.bfloat16) for _ in range(3)]
+        binding.bwd(q, k, v, out.view(bh, S, hd), do, lse.view(bh, S), scale, impl,
+                    grads=tuple(g[1].view(bh, S, hd) for g in grads))
+        torch.cuda.synchronize()
+        for buf in [bo, bl] + [g[0] for g in grads]:
+            assert torch.all(buf[:guard] == -7.0) and torch.all(buf[-guard:] == -7.0)
+
+
+def test_backward_is_repeatable_with_reused_workspace():
+    from bwd_xfa_fwd_gb300 import binding
+    bh, S, hd = 4, 512, 128
+    x = inputs.draw((bh, S, hd), "bf16", seed=12)
+    q, k, v, do = (to_device(x[n], "bf16") for n in ("q", "k", "v", "dout"))
+    out, lse = binding.fwd(q, k, v)
+    ws = torch.empty(binding.workspace_bytes(bh, S, hd, torch.bfloat16), device="cuda", dtype=torch.uint8)
+    a = binding.bwd(q, k, v, out, do, lse, workspace=ws)
+    a = [t.clone() for t in a]
+    b = binding.bwd(q, k, v, out, do, lse, workspace=ws)
+    for s, t in zip(a, b):
+        # dQ is summed with fp32 atomics in a data-dependent order: equal up to rounding
+        assert torch.allclose(s.float(), t.float(), rtol=0, atol=1e-2 * float(s.float().abs().max()))
+
+
+def test_unsupported_combinations_are_rejected():
+    from bwd_xfa_fwd_gb300 import binding
+    t = torch.zeros(1, 64, 32, device="cuda")
+    with pytest.raises(binding.XfaError) as e:
+        binding.fwd(t, t, t, impl=binding.IMPL_TCGEN05)
+    assert e.value.code == binding.XFA_ERR_UNSUPPORTED
+
+
+def test_timeout_path_reports_and_recovers():
+    from bwd_xfa_fwd_gb300 import binding
+    assert binding.status() == binding.XFA_OK
+    assert binding.selftest_timeout(2000) == binding.XFA_OK
+    assert binding.status() == binding.XFA_ERR_TIMEOUT
+    assert binding.status() == binding.XFA_OK       # cleared
+    w = inputs.WORKLOADS[1]
+    x = inputs.workload_inputs(w)
+    compare(run_gpu(x, w.dtype, w.scale), oracle_result(("w", 1), x, w.scale), w.dtype)   # context still usable
+
+
+def test_tape_node_fanout_on_gpu():
+    """out = flash_attention(x, x, x): the tape sums dQ + dK + dV into x.grad."""
+    from bwd_xfa_fwd_gb300.tape import Var, flash_attention
+    bh, S, hd = 2, 200, 64
+    scale = 1.0 / math.sqrt(hd)
+    xin = inputs.draw((bh, S, hd), "bf16", seed=21, names=("x", "w"))
+    xv = Var(to_device(xin["x"], "bf16"))
+    y = flash_attention(xv, xv, xv, scale)
+    y.backward(seed=to_device(xin["w"], "bf16"))
+    ref = oracle_result(("tape",), {"q": xin["x"], "k": xin["x"], "v": xin["x"], "dout": xin["w"]}, scale)
+    got = {"out": to_f64(y.value), "dq": to_f64(xv.grad)}
+    want = {"out": ref["out"], "dq": ref["dq"] + ref["dk"] + ref["dv"]}
+    compare(got, want, "bf16", names=("out", "dq"))
