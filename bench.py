@@ -105,7 +105,7 @@ def make_device_inputs(w, torch):
     return x, dev
 
 
-def cpu_baseline_leg(w, heads=(0, 1)):
+def cpu_baseline_leg(w, heads=tuple(range(8))):
     """The oracle as it stands, on all host cores, on a bounded sample: the
     forward + backward of ``heads`` of the full-size workload."""
     import oracle

@@ -20,9 +20,10 @@
 //       dQ^T = K_j^T dS^T           (M=hd, N=64, K=128 keys)       -> TMEM
 //   * warps 0-3 (thread = key) turn S^T, dP^T into P^T (bf16, back into the
 //     S^T columns) and dS^T (bf16, swizzled smem);
-//   * warps 4-7 (thread = hd index) read dQ^T and add it into the fp32 dQ
-//     accumulator in global memory with coalesced reductions (32 consecutive
-//     floats per warp instruction); a conversion kernel writes dQ afterwards.
+//   * warps 4-7 (thread = hd index) read dQ^T from TMEM, stage it as a
+//     row-major fp32 [64][hd] tile in shared memory (one contiguous block of
+//     the [S][hd] accumulator) and add it into global memory with a single
+//     TMA bulk reduce-add; a conversion kernel writes dQ afterwards.
 // TMEM map (512 columns): dK [0,hd) dV [hd,2hd) S^T x2 [2hd,2hd+128)
 //                         dP^T [2hd+128,2hd+192) dQ^T [2hd+192,2hd+256).
 // For hd = 64 the dQ^T MMA still runs with M = 128; lanes 64-127 hold
@@ -55,7 +56,8 @@ struct Cfg {
     static constexpr int OFF_Q = 2 * KV_BYTES;
     static constexpr int OFF_DO = OFF_Q + NSQ * Q_BYTES;
     static constexpr int OFF_DS = OFF_DO + NSQ * Q_BYTES;
-    static constexpr int OFF_LD = OFF_DS + 2 * DS_BYTES;  // per stage: Lg[64], D[64]
+    static constexpr int OFF_DQ = OFF_DS + 2 * DS_BYTES;  // fp32 dQ tile [64 rows][hd] staged for the bulk reduce
+    static constexpr int OFF_LD = OFF_DQ + BM * HD * 4;   // per stage: Lg[64], D[64]
     static constexpr int OFF_BAR = OFF_LD + NSQ * 2 * BM * 4;
     static constexpr int SMEM = OFF_BAR + 512 + 1024;
     static constexpr uint32_t COL_DK = 0, COL_DV = HD, COL_S = 2 * HD, COL_DP = 2 * HD + 128,
@@ -112,6 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Bars *bars = reinterpret_cast<Bars *>(smem + C::OFF_BAR);
     float *ld_s = reinterpret_cast<float *>(smem + C::OFF_LD);
+    float *dq_stage = reinterpret_cast<float *>(smem + C::OFF_DQ);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     const int jt = (int)(blockIdx.x / bh);        // key tile: low tiles have the most work, go first
@@ -363,12 +366,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before_sync();
                 mbar_arrive(&bars->dq_empty);
                 const int i0 = (it0 + it) * BM;
-                float *dst = dq_acc + ((size_t)head * S + i0) * HD + d;
                 const int rows = min(BM, S - i0);
-#pragma unroll 8
-                for (int c = 0; c < BM; ++c)
-                    if (c < rows) atomicAdd(dst + (size_t)c * HD, __uint_as_float(g[c]));
+                // the staging tile is free once the previous bulk reduce has read it
+                if (d == 0) bulk_wait_group_read0();
+                named_bar_sync(1, HD);
+#pragma unroll
+                for (int c = 0; c < BM; ++c) dq_stage[c * HD + d] = __uint_as_float(g[c]);
+                fence_proxy_async_smem();
+                named_bar_sync(1, HD);
+                if (d == 0) {
+                    bulk_reduce_add_f32(dq_acc + ((size_t)head * S + i0) * HD, dq_stage, (uint32_t)(rows * HD * 4));
+                    bulk_commit_group();
+                }
             }
+            if (d == 0) bulk_wait_group0();
         }
         // epilogue: dK rows (same TMEM lanes as warps 0-3: thread = key)
         const int key = j0 + wq * 32 + lane;
