@@ -137,6 +137,37 @@ int xfa_bwd_finish(void *dq, int bh, int S, int hd, int dtype, void *workspace, 
                    void *stream);
 
 /*
+ * Size in bytes of the fixed device scratch array used by xfa_bwd_noalloc.
+ * It covers xfa_bwd_workspace_bytes() up to 32 MiB, i.e. bf16 bh*S*hd up to
+ * about 8 million elements at hd = 128 (bh = 32, S = 1024 needs 16.25 MiB).
+ */
+#define XFA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * xfa_bwd for callers that cannot allocate device memory when they run the
+ * backward (a host framework that has reserved the device memory for its own
+ * allocator, a plug-in host that forbids allocation in its callbacks, code
+ * that cannot take cudaMalloc's implicit device synchronisation).  The pages
+ * have no counterpart: this is a deployment variant of xfa_bwd, not part of
+ * the method.
+ *   Arguments as xfa_bwd, without the workspace: the scratch is one
+ *   file-scope device array of XFA_NOALLOC_SCRATCH_BYTES inside the library,
+ *   held by every GPU that loads it until the process exits.
+ *   Returns XFA_ERR_WORKSPACE when xfa_bwd_workspace_bytes() for the shape
+ *   exceeds XFA_NOALLOC_SCRATCH_BYTES; otherwise as xfa_bwd.
+ *   Allocates nothing (no cudaMalloc/cudaFree or allocating library call).
+ *   The first call on a device, made with that device current, resolves the
+ *   array's device address (cudaGetSymbolAddress); make that first call
+ *   before any stream capture.
+ *   Every call shares the array and it keeps the last call's contents (each
+ *   call rewrites or clears everything it reads before reading it); calls
+ *   that overlap on the GPU race on it.
+ */
+int xfa_bwd_noalloc(const void *q, const void *k, const void *v, const void *out, const void *dout,
+                    const float *lse, void *dq, void *dk, void *dv,
+                    int bh, int S, int hd, float scale, int dtype, void *stream);
+
+/*
  * The backward's pre-pass on its own: D[b][i] = sum_d dout[b][i][d] * out[b][i][d]
  * with fp32 accumulation.  Passage: "xtrain docs/13-flash-attention.md",
  * design decision ③ (D_i = sum_d dO_i[d] O_i[d]).
