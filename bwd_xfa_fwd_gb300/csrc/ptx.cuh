@@ -211,6 +211,18 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// One lane of a converged warp is elected (elect.sync); returns true in that lane only.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.b32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A/B, fp32 accumulator, M x N tile.
 // a_mn / b_mn select MN-major (transposed) operand layouts in shared memory.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn)
@@ -223,6 +235,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
            | ((uint32_t)(N >> 3) << 17)    // N / 8
            | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
+
+// Advance a shared-memory descriptor's start address by `bytes` (a multiple of 16;
+// the address field holds bytes >> 4 and shared-memory addresses stay below 256 KB).
+__host__ __device__ constexpr uint64_t sdesc_advance(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.
 //   K-major: rows of 128 B (64 bf16 along K), 8-row groups `sbo` bytes apart.

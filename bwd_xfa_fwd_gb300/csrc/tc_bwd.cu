@@ -39,12 +39,14 @@ namespace {
 
 constexpr int BN = 128;       // keys per CTA (MMA M)
 constexpr int BM = 64;        // query rows per tile (MMA N of S^T / dP^T)
-constexpr int NSQ = 2;        // query-tile ring depth
+template <int HD>
+constexpr int ring_depth() { return HD == 128 ? 3 : 4; }   // query-tile (Q, dO, L, D) ring stages
 constexpr int kThreads = 320;
 constexpr int kWarpTma = 8, kWarpMma = 9;
 
 template <int HD>
 struct Cfg {
+    static constexpr int NSQ = ring_depth<HD>();
     static constexpr int SUB = HD / 64;
     static constexpr int KV_SUB = BN * 128;             // 128 rows x 128 B
     static constexpr int Q_SUB = BM * 128;              // 64 rows x 128 B
@@ -59,15 +61,17 @@ struct Cfg {
     static constexpr int OFF_DQ = OFF_DS + 2 * DS_BYTES;  // fp32 dQ tile [64 rows][hd] staged for the bulk reduce
     static constexpr int OFF_LD = OFF_DQ + BM * HD * 4;   // per stage: Lg[64], D[64]
     static constexpr int OFF_BAR = OFF_LD + NSQ * 2 * BM * 4;
-    static constexpr int SMEM = OFF_BAR + 512 + 1024;
+    static constexpr int SMEM = OFF_BAR + 256 + 1024;   // barriers + alignment slack
     static constexpr uint32_t COL_DK = 0, COL_DV = HD, COL_S = 2 * HD, COL_DP = 2 * HD + 128,
                               COL_DQ = 2 * HD + 192;
     static constexpr uint32_t TMEM_COLS = 512;
 };
 
+constexpr int kMaxRing = 4;
+
 struct Bars {
     uint64_t kv_full;
-    uint64_t q_full[NSQ], q_empty[NSQ];
+    uint64_t q_full[kMaxRing], q_empty[kMaxRing];
     uint64_t s_full[2], p_full[2], ds_full[2], ds_empty[2];
     uint64_t dp_full, dq_full, dq_empty, done, drain;
     uint32_t tmem_base;
@@ -88,16 +92,17 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, Bars *
     return ok;
 }
 
-// C[M=128, N=64] = A[128 rows x hd] * B[64 rows x hd]^T, both K-major (hd contiguous).
+// C[M=128, N=64] = A[128 rows x hd] * B[64 rows x hd]^T, both K-major (hd contiguous);
+// descriptors of the tile bases, advanced per 16-wide K step.
 template <int HD>
-__device__ __forceinline__ void issue_rows_dot(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem)
+__device__ __forceinline__ void issue_rows_dot(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc)
 {
     constexpr uint32_t idesc = idesc_bf16(BN, BM, false, false);
 #pragma unroll
     for (int ks = 0; ks < HD / 16; ++ks) {
         const uint32_t k_off = (ks % 4) * 32;
-        mma_ss(d_tmem, sdesc_sw128(a_smem + (ks / 4) * Cfg<HD>::KV_SUB + k_off, 16, 1024),
-               sdesc_sw128(b_smem + (ks / 4) * Cfg<HD>::Q_SUB + k_off, 16, 1024), idesc, ks > 0);
+        mma_ss(d_tmem, sdesc_advance(a_desc, (ks / 4) * Cfg<HD>::KV_SUB + k_off),
+               sdesc_advance(b_desc, (ks / 4) * Cfg<HD>::Q_SUB + k_off), idesc, ks > 0);
     }
 }
 
@@ -110,6 +115,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   float scale, float scale_log2, int *status)
 {
     using C = Cfg<HD>;
+    constexpr int NSQ = C::NSQ;
+    static_assert(NSQ <= kMaxRing && sizeof(Bars) <= 256, "barrier block");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Bars *bars = reinterpret_cast<Bars *>(smem + C::OFF_BAR);
@@ -164,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(smem + C::OFF_K + s * C::KV_SUB, &tm_k, &bars->kv_full, s * 64, j0, head);
                 tma_load_3d(smem + C::OFF_V + s * C::KV_SUB, &tm_v, &bars->kv_full, s * 64, j0, head);
             }
-            int issued[NSQ] = {0, 0};
+            int issued[NSQ] = {};
             for (int it = 0; it < n; ++it) {
                 const int st = it % NSQ;
                 if (it >= NSQ && !mbar_wait(&bars->q_empty[st], ((it / NSQ) + 1) & 1, &bars->abort)) {
@@ -189,65 +196,89 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (issued[st]) mbar_wait(&bars->q_full[st], ((issued[st] - 1) / NSQ) & 1, nullptr);
         }
     } else if (warp == kWarpMma) {
-        if (lane == 0) {
-            const uint32_t k_s = smem_u32(smem + C::OFF_K), v_s = smem_u32(smem + C::OFF_V);
-            const uint32_t q_s = smem_u32(smem + C::OFF_Q), do_s = smem_u32(smem + C::OFF_DO);
-            const uint32_t ds_s = smem_u32(smem + C::OFF_DS);
-            constexpr uint32_t idesc_acc = idesc_bf16(BN, HD, false, true);    // dV, dK: B MN-major
-            constexpr uint32_t idesc_dq = idesc_bf16(128, BM, true, true);     // dQ^T: A, B MN-major
-            bool ok = mbar_wait(&bars->kv_full, 0, &bars->abort) && mbar_wait(&bars->q_full[0], 0, &bars->abort);
-            if (ok) {
-                tc_fence_after_sync();
-                issue_rows_dot<HD>(tmem + C::COL_S, k_s, q_s);
+        // The whole warp runs the issue loop (converged, descriptors warp-uniform);
+        // one elected lane issues the tcgen05 instructions.
+        const bool leader = elect_one();
+        const uint32_t k_s = smem_u32(smem + C::OFF_K), v_s = smem_u32(smem + C::OFF_V);
+        const uint32_t q_s = smem_u32(smem + C::OFF_Q), do_s = smem_u32(smem + C::OFF_DO);
+        const uint32_t ds_s = smem_u32(smem + C::OFF_DS);
+        // K-major views (hd contiguous) for S^T = K Q^T and dP^T = V dO^T
+        const uint64_t k_km = sdesc_sw128(k_s, 16, 1024), v_km = sdesc_sw128(v_s, 16, 1024);
+        const uint64_t q_km = sdesc_sw128(q_s, 16, 1024), do_km = sdesc_sw128(do_s, 16, 1024);
+        // MN-major views: B = dO_i / Q_i for dV / dK, A = K_j^T for dQ^T; dS^T as K-major A / MN-major B
+        const uint64_t do_mn = sdesc_sw128(do_s, C::Q_SUB, 1024), q_mn = sdesc_sw128(q_s, C::Q_SUB, 1024);
+        const uint64_t k_mn = sdesc_sw128(k_s, C::KV_SUB, 1024);
+        const uint64_t ds_km = sdesc_sw128(ds_s, 16, 1024), ds_mn = sdesc_sw128(ds_s, C::DS_BYTES, 1024);
+        constexpr uint32_t idesc_acc = idesc_bf16(BN, HD, false, true);    // dV, dK: B MN-major
+        constexpr uint32_t idesc_dq = idesc_bf16(128, BM, true, true);     // dQ^T: A, B MN-major
+        bool ok = warp_wait(&bars->kv_full, 0, bars, status) && warp_wait(&bars->q_full[0], 0, bars, status);
+        if (ok) {
+            tc_fence_after_sync();
+            if (leader) {
+                issue_rows_dot<HD>(tmem + C::COL_S, k_km, q_km);
                 tc_commit(&bars->s_full[0]);
-                issue_rows_dot<HD>(tmem + C::COL_DP, v_s, do_s);
+                issue_rows_dot<HD>(tmem + C::COL_DP, v_km, do_km);
                 tc_commit(&bars->dp_full);
             }
-            for (int it = 0; ok && it < n; ++it) {
-                const int b = it & 1, st = it % NSQ;
-                const uint32_t ph2 = (it >> 1) & 1;
-                const uint32_t qs = q_s + st * C::Q_BYTES, dos = do_s + st * C::Q_BYTES;
-                const uint32_t dsb = ds_s + b * C::DS_BYTES;
-                const int nx = it + 1, stn = nx % NSQ;
-                if (nx < n) {   // S^T of the next tile into the other buffer (its P was consumed in order)
-                    if (!(ok = mbar_wait(&bars->q_full[stn], (nx / NSQ) & 1, &bars->abort))) break;
-                    tc_fence_after_sync();
-                    issue_rows_dot<HD>(tmem + C::COL_S + 64 * (nx & 1), k_s, q_s + stn * C::Q_BYTES);
+            __syncwarp();
+        }
+        for (int it = 0; ok && it < n; ++it) {
+            const int b = it & 1, st = it % NSQ;
+            const uint32_t ph2 = (it >> 1) & 1;
+            const uint32_t qoff = st * C::Q_BYTES, dsoff = b * C::DS_BYTES;
+            const int nx = it + 1, stn = nx % NSQ;
+            if (nx < n) {   // S^T of the next tile into the other buffer (its P was consumed in order)
+                if (!(ok = warp_wait(&bars->q_full[stn], (nx / NSQ) & 1, bars, status))) break;
+                tc_fence_after_sync();
+                if (leader) {
+                    issue_rows_dot<HD>(tmem + C::COL_S + 64 * (nx & 1), k_km, sdesc_advance(q_km, stn * C::Q_BYTES));
                     tc_commit(&bars->s_full[nx & 1]);
                 }
-                // dV += P^T dO_i  (P^T: bf16 in the S^T columns of buffer b)
-                if (!(ok = mbar_wait(&bars->p_full[b], ph2, &bars->abort))) break;
-                tc_fence_after_sync();
+                __syncwarp();
+            }
+            // dV += P^T dO_i  (P^T: bf16 in the S^T columns of buffer b)
+            if (!(ok = warp_wait(&bars->p_full[b], ph2, bars, status))) break;
+            tc_fence_after_sync();
+            if (leader) {
 #pragma unroll
                 for (int ks = 0; ks < BM / 16; ++ks)
                     mma_ts(tmem + C::COL_DV, tmem + C::COL_S + 64 * b + ks * 8,
-                           sdesc_sw128(dos + ks * 2048, C::Q_SUB, 1024), idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
-                // dS^T is in smem and dP^T has been read: next dP^T first, then dK and dQ^T
-                if (!(ok = mbar_wait(&bars->ds_full[b], ph2, &bars->abort))) break;
-                tc_fence_after_sync();
+                           sdesc_advance(do_mn, qoff + ks * 2048), idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
+            }
+            __syncwarp();
+            // dS^T is in smem and dP^T has been read: next dP^T first, then dK and dQ^T
+            if (!(ok = warp_wait(&bars->ds_full[b], ph2, bars, status))) break;
+            tc_fence_after_sync();
+            if (leader) {
                 if (nx < n) {
-                    issue_rows_dot<HD>(tmem + C::COL_DP, v_s, do_s + stn * C::Q_BYTES);
+                    issue_rows_dot<HD>(tmem + C::COL_DP, v_km, sdesc_advance(do_km, stn * C::Q_BYTES));
                     tc_commit(&bars->dp_full);
                 }
 #pragma unroll
                 for (int ks = 0; ks < BM / 16; ++ks)
-                    mma_ss(tmem + C::COL_DK, sdesc_sw128(dsb + ks * 32, 16, 1024),
-                           sdesc_sw128(qs + ks * 2048, C::Q_SUB, 1024), idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
+                    mma_ss(tmem + C::COL_DK, sdesc_advance(ds_km, dsoff + ks * 32), sdesc_advance(q_mn, qoff + ks * 2048),
+                           idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
                 tc_commit(&bars->q_empty[st]);
-                if (it > 0 && !(ok = mbar_wait(&bars->dq_empty, (it - 1) & 1, &bars->abort))) break;
-                tc_fence_after_sync();
+            }
+            __syncwarp();
+            if (it > 0 && !(ok = warp_wait(&bars->dq_empty, (it - 1) & 1, bars, status))) break;
+            tc_fence_after_sync();
+            if (leader) {
 #pragma unroll
                 for (int ks = 0; ks < BN / 16; ++ks)
-                    mma_ss(tmem + C::COL_DQ, sdesc_sw128(k_s + ks * 2048, C::KV_SUB, 1024),
-                           sdesc_sw128(dsb + ks * 2048, C::DS_BYTES, 1024), idesc_dq, ks > 0 ? 1u : 0u);
+                    mma_ss(tmem + C::COL_DQ, sdesc_advance(k_mn, ks * 2048), sdesc_advance(ds_mn, dsoff + ks * 2048),
+                           idesc_dq, ks > 0 ? 1u : 0u);
                 tc_commit(&bars->dq_full);
                 tc_commit(&bars->ds_empty[b]);
             }
+            __syncwarp();
+        }
+        if (leader) {
             if (ok) tc_commit(&bars->done);
-            else fail(bars, status);
             tc_commit(&bars->drain);
             mbar_wait(&bars->drain, 0, nullptr);
         }
+        __syncwarp();
     } else if (warp < 4) {
         // thread = key row r of this CTA (TMEM lane)
         const int r = warp * 32 + lane;
@@ -424,6 +455,7 @@ int run(const BwdParams &p, cudaStream_t st)
     if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tq, p.q, HD, p.S, p.bh, BM);
     if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tdo, p.dout, HD, p.S, p.bh, BM);
     if (rc != XFA_OK) return rc;
+    static_assert(Cfg<HD>::SMEM <= 227 * 1024, "shared memory per CTA");
     auto kern = tc_bwd_kernel<HD>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<HD>::SMEM);
     if (e != cudaSuccess) return XFA_ERR_CUDA_BASE + (int)e;

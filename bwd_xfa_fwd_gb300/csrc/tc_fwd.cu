@@ -83,27 +83,26 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, Bars *
     return ok;
 }
 
+// S = Q K^T: M=128, N=128, K=hd in steps of 16 (K-major, 128-byte swizzle; 64-column blocks SUB_BYTES apart).
 template <int HD>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem)
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc)
 {
     constexpr uint32_t idesc = idesc_bf16(BM, BN, false, false);
 #pragma unroll
     for (int ks = 0; ks < HD / 16; ++ks) {
         const uint32_t off = (ks / 4) * Cfg<HD>::SUB_BYTES + (ks % 4) * 32;
-        mma_ss(d_tmem, sdesc_sw128(q_smem + off, 16, 1024), sdesc_sw128(k_smem + off, 16, 1024), idesc, ks > 0);
+        mma_ss(d_tmem, sdesc_advance(q_desc, off), sdesc_advance(k_desc, off), idesc, ks > 0);
     }
 }
 
+// O += P V: P (bf16) from TMEM, V [keys][hd] as an MN-major B operand; 16 keys = 2048 bytes.
 template <int HD>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem, bool accumulate)
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, bool accumulate)
 {
     constexpr uint32_t idesc = idesc_bf16(BM, HD, false, true);
 #pragma unroll
-    for (int ks = 0; ks < BN / 16; ++ks) {
-        // V is [keys][hd]: MN-major B operand; 16 keys = 2048 bytes, hd blocks of 64 are SUB_BYTES apart.
-        mma_ts(o_tmem, p_tmem + ks * 8, sdesc_sw128(v_smem + ks * 2048, Cfg<HD>::SUB_BYTES, 1024), idesc,
-               (accumulate || ks > 0) ? 1u : 0u);
-    }
+    for (int ks = 0; ks < BN / 16; ++ks)
+        mma_ts(o_tmem, p_tmem + ks * 8, sdesc_advance(v_desc, ks * 2048), idesc, (accumulate || ks > 0) ? 1u : 0u);
 }
 
 template <int HD>
@@ -123,8 +122,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int head = (int)(blockIdx.x % bh);
     const int q0 = qb * 2 * BM;
     const bool t1 = q0 + BM < S;
-    const int n_t[2] = {2 * qb + 1, t1 ? 2 * qb + 2 : 0};   // key tiles per query tile
-    const int nkv = t1 ? n_t[1] : n_t[0];
+    const int n_t0 = 2 * qb + 1, n_t1 = t1 ? 2 * qb + 2 : 0;   // key tiles per query tile
+    const int nkv = t1 ? n_t1 : n_t0;
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
@@ -192,49 +191,70 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == kWarpMma) {
-        if (lane == 0) {
-            const uint32_t q_s[2] = {smem_u32(smem + C::OFF_Q0), smem_u32(smem + C::OFF_Q1)};
-            const uint32_t k_s = smem_u32(smem + C::OFF_K), v_s = smem_u32(smem + C::OFF_V);
-            bool ok = mbar_wait(&bars->q_full, 0, &bars->abort) && mbar_wait(&bars->k_full[0], 0, &bars->abort);
-            if (ok) {
-                tc_fence_after_sync();
-                for (int t = 0; t < 2; ++t) {
-                    if (n_t[t] == 0) continue;
-                    issue_qk<HD>(tmem + C::col_s(t), q_s[t], k_s);
-                    tc_commit(&bars->s_full[t]);
+        // The whole warp runs the issue loop (converged, so descriptors stay warp-uniform);
+        // one elected lane issues the tcgen05 instructions.
+        const bool leader = elect_one();
+        const uint64_t q_desc[2] = {sdesc_sw128(smem_u32(smem + C::OFF_Q0), 16, 1024),
+                                    sdesc_sw128(smem_u32(smem + C::OFF_Q1), 16, 1024)};
+        const uint64_t k_desc = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);
+        const uint64_t v_desc = sdesc_sw128(smem_u32(smem + C::OFF_V), C::SUB_BYTES, 1024);
+        bool ok = warp_wait(&bars->q_full, 0, bars, status) && warp_wait(&bars->k_full[0], 0, bars, status);
+        if (ok) {
+            tc_fence_after_sync();
+            if (leader) {
+                issue_qk<HD>(tmem + C::col_s(0), q_desc[0], k_desc);
+                tc_commit(&bars->s_full[0]);
+                if (t1) {
+                    issue_qk<HD>(tmem + C::col_s(1), q_desc[1], k_desc);
+                    tc_commit(&bars->s_full[1]);
                 }
                 tc_commit(&bars->k_empty[0]);
             }
-            for (int j = 0; ok && j < nkv; ++j) {
-                const int st = j % C::NS;
-                const uint32_t ph = (j / C::NS) & 1;
-                bool v_ready = false, k_next_ready = false;
-                const int jn = j + 1, stn = jn % C::NS;
-                const uint32_t phn = (jn / C::NS) & 1;
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (j >= n_t[t]) continue;
-                    ok = mbar_wait(&bars->p_full[t], j & 1, &bars->abort);
-                    if (ok && !v_ready) ok = v_ready = mbar_wait(&bars->v_full[st], ph, &bars->abort);
+            __syncwarp();
+        }
+        for (int j = 0; ok && j < nkv; ++j) {
+            const int st = j % C::NS;
+            const uint32_t ph = (j / C::NS) & 1;
+            bool v_ready = false, k_next_ready = false;
+            const int jn = j + 1, stn = jn % C::NS;
+            const uint32_t phn = (jn / C::NS) & 1;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int nt = t == 0 ? n_t0 : n_t1;
+                if (j >= nt) continue;
+                ok = warp_wait(&bars->p_full[t], j & 1, bars, status);
+                if (ok && !v_ready) ok = v_ready = warp_wait(&bars->v_full[st], ph, bars, status);
+                if (!ok) break;
+                tc_fence_after_sync();
+                if (leader) {
+                    issue_pv<HD>(tmem + C::col_o(t), tmem + C::col_s(t), sdesc_advance(v_desc, st * C::TILE_BYTES),
+                                 j > 0);
+                    if (j == nt - 1) tc_commit(&bars->o_full[t]);
+                }
+                __syncwarp();
+                if (jn < nt) {
+                    if (!k_next_ready) ok = k_next_ready = warp_wait(&bars->k_full[stn], phn, bars, status);
                     if (!ok) break;
                     tc_fence_after_sync();
-                    issue_pv<HD>(tmem + C::col_o(t), tmem + C::col_s(t), v_s + st * C::TILE_BYTES, j > 0);
-                    if (j == n_t[t] - 1) tc_commit(&bars->o_full[t]);
-                    if (jn < n_t[t]) {
-                        if (!k_next_ready) ok = k_next_ready = mbar_wait(&bars->k_full[stn], phn, &bars->abort);
-                        if (!ok) break;
-                        tc_fence_after_sync();
-                        issue_qk<HD>(tmem + C::col_s(t), q_s[t], k_s + stn * C::TILE_BYTES);
+                    if (leader) {
+                        issue_qk<HD>(tmem + C::col_s(t), q_desc[t], sdesc_advance(k_desc, stn * C::TILE_BYTES));
                         tc_commit(&bars->s_full[t]);
                     }
+                    __syncwarp();
                 }
-                if (!ok) break;
+            }
+            if (!ok) break;
+            if (leader) {
                 if (k_next_ready) tc_commit(&bars->k_empty[stn]);
                 tc_commit(&bars->v_empty[st]);
             }
-            if (!ok) fail(bars, status);
+            __syncwarp();
+        }
+        if (leader) {
             tc_commit(&bars->drain);
             mbar_wait(&bars->drain, 0, nullptr);
         }
+        __syncwarp();
     } else {
         // softmax group of tile t; thread = query row
         const int t = warp / 4, wq = warp % 4;
@@ -246,7 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_off + C::col_o(t);
         float m = -CUDART_INF_F, l = 0.0f;
         bool ok = true;
-        for (int j = 0; j < n_t[t]; ++j) {
+        const int n_mine = t == 0 ? n_t0 : n_t1;
+        for (int j = 0; j < n_mine; ++j) {
             if (!(ok = warp_wait(&bars->s_full[t], j & 1, bars, status))) break;
             tc_fence_after_sync();
             uint32_t sr[128];
@@ -259,18 +280,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             reg_fence32(sr + 32);
             reg_fence32(sr + 64);
             reg_fence32(sr + 96);
-            float x[128];
-#pragma unroll
-            for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]) * scale_log2;
+            // raw scores; the diagonal tile masks keys past the row
             if (j == diag) {
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
-                    if (c > r) x[c] = -CUDART_INF_F;
+                    if (c > r) sr[c] = 0xff800000u;   // -inf
             }
-            float mx = x[0];
+            // row max with 8 independent partial maxima (short dependency chains)
+            float mx8[8];
 #pragma unroll
-            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
-            const float m_new = fmaxf(m, mx);
+            for (int e = 0; e < 8; ++e) mx8[e] = __uint_as_float(sr[e]);
+#pragma unroll
+            for (int c = 8; c < 128; c += 8)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], __uint_as_float(sr[c + e]));
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            const float m_new = fmaxf(m, mx * scale_log2);   // scale > 0: max commutes with the scaling
             const bool need = m_new > m + kRescaleThreshold;
             if (__any_sync(0xffffffffu, need)) {
                 const float alpha = ex2_approx(m - m_new);   // 0 on the first tile
@@ -290,23 +316,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 m = m_new;
             }
+            // p = 2^(s * scale * log2(e) - m): one FFMA + one ex2 per score; 8 partial row sums
+            const float neg_m = -m;
+            float l8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) l8[e] = 0.0f;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float p0 = ex2_approx(x[64 * h + 2 * e] - m);
-                    const float p1 = ex2_approx(x[64 * h + 2 * e + 1] - m);
-                    l += p0 + p1;
+                    const int c = 64 * h + 2 * e;
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), scale_log2, neg_m));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), scale_log2, neg_m));
+                    l8[(2 * e) & 7] += p0;
+                    l8[(2 * e + 1) & 7] += p1;
                     pk[e] = pack_bf16x2(p0, p1);
                 }
                 tmem_st32(tS + 32 * h, pk);
             }
+            l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
             tmem_wait_st();
             tc_fence_before_sync();
             mbar_arrive(&bars->p_full[t]);
         }
-        if (ok && n_t[t] > 0 && warp_wait(&bars->o_full[t], 0, bars, status)) {
+        if (ok && n_mine > 0 && warp_wait(&bars->o_full[t], 0, bars, status)) {
             tc_fence_after_sync();
             const float inv_l = 1.0f / l;
             __nv_bfloat16 *orow = O + ((size_t)head * S + row) * HD;
@@ -349,6 +383,7 @@ int run(const FwdParams &p, cudaStream_t st)
     if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tk, p.k, HD, p.S, p.bh, BN);
     if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tv, p.v, HD, p.S, p.bh, BN);
     if (rc != XFA_OK) return rc;
+    static_assert(Cfg<HD>::SMEM <= 227 * 1024, "shared memory per CTA");
     auto kern = tc_fwd_kernel<HD>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<HD>::SMEM);
     if (e != cudaSuccess) return XFA_ERR_CUDA_BASE + (int)e;
