@@ -1,7 +1,7 @@
 // Bandwidth kernels around the attention kernels:
 //   - the backward pre-pass D_i = sum_d dO_i[d] O_i[d]
 //     ("xtrain docs/13-flash-attention.md", design decision ③), fused with
-//     the conversion of L to base 2, the padding of both arrays to whole
+//     the conversion of L to -L*log2(e), the padding of both arrays to whole
 //     query tiles (so the backward kernels can bulk-copy them per tile) and
 //     the clearing of the fp32 dQ accumulator;
 //   - the fp32 dQ accumulator -> output dtype conversion;
@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(256) rowdot_kernel(const VecT *__restrict__ O,
         for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (valid && sub == 0) {
             D[r] = acc;
-            if (PREP) Lg[r] = real ? lse[b * S + i] * kLog2e : CUDART_INF_F;
+            if (PREP) Lg[r] = real ? -lse[b * S + i] * kLog2e : -CUDART_INF_F;
         }
         if (PREP && real && zero_acc) {
             // clear this row of the fp32 dQ accumulator: HD floats over the LPR lanes of the row

@@ -28,7 +28,7 @@ struct BwdParams {
     int dtype;
     // workspace views
     float *D;       // [bh][S_pad]  D_i = dO_i . O_i (0 on padded rows)
-    float *Lg;      // [bh][S_pad]  L_i * log2(e) (+inf on padded rows)
+    float *Lg;      // [bh][S_pad]  -L_i * log2(e) (-inf on padded rows)
     float *dq_acc;  // [bh][S][hd]  fp32 dQ accumulator (== dq when dtype is fp32)
     int S_pad;
     int *status;
@@ -41,7 +41,7 @@ constexpr int kRowPad = 128;
 cudaError_t launch_simt_fwd(const FwdParams &p, cudaStream_t st);
 cudaError_t launch_simt_bwd(const BwdParams &p, cudaStream_t st);
 
-// Backward pre-pass: D = rowdot(dO, O), Lg = lse * log2(e), padded rows filled.
+// Backward pre-pass: D = rowdot(dO, O), Lg = -lse * log2(e), padded rows filled.
 cudaError_t launch_bwd_prep(const BwdParams &p, cudaStream_t st);
 // Plain rowdot into an unpadded [bh][S] array.
 cudaError_t launch_rowdot(const void *out, const void *dout, float *d, int bh, int S, int hd, int dtype,

@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(const T *__restrict_
             for (int j = 0; j < 4; ++j) {
                 const int r = sr0 + i, c = sc + 16 * j;
                 const bool masked = (k0 + c) > (q0 + r);
-                const float p = masked ? 0.0f : exp2f(s[i][j] * scale_log2 - Ls[r]);
+                const float p = masked ? 0.0f : exp2f(fmaf(s[i][j], scale_log2, Ls[r]));
                 Ps[r * (kTile + 1) + c] = p;
                 dSs[r * (kTile + 1) + c] = p * (dp[i][j] - Ds[r]) * scale;
             }

@@ -10,7 +10,7 @@
 //   * a CTA owns 128 keys of one head; K_j and V_j are loaded once by TMA and
 //     dK_j, dV_j accumulate in TMEM (128 lanes = keys, hd fp32 columns each)
 //     over every 64-row query tile at or below the diagonal;
-//   * warp 8 streams Q_i, dO_i (TMA, 128-byte swizzle) with L_i*log2(e) and
+//   * warp 8 streams Q_i, dO_i (TMA, 128-byte swizzle) with -L_i*log2(e) and
 //     D_i (bulk copies) through a ring;
 //   * warp 9 (one thread) issues, per query tile:
 //       S^T  = K_j Q_i^T            (M=128 keys, N=64 rows, K=hd)  -> TMEM, double buffered
@@ -139,13 +139,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars->s_full[b], 1);
-            mbar_init(&bars->p_full[b], 128);
-            mbar_init(&bars->ds_full[b], 128);
+            mbar_init(&bars->p_full[b], 4);    // one arrival per key warp
+            mbar_init(&bars->ds_full[b], 4);
             mbar_init(&bars->ds_empty[b], 1);
         }
         mbar_init(&bars->dp_full, 1);
         mbar_init(&bars->dq_full, 1);
-        mbar_init(&bars->dq_empty, HD);
+        mbar_init(&bars->dq_empty, HD / 32);   // one arrival per readout warp
         mbar_init(&bars->done, 1);
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
@@ -299,33 +299,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
             reg_fence32(sr);
             reg_fence32(sr + 32);
-            float p[64];
+            // p = 2^(s * scale * log2(e) - L * log2(e)) on packed pairs; -L*log2(e) comes from the pre-pass
+            const uint64_t cs2 = f2_pack(scale_log2, scale_log2);
             const bool diag = key > i0;   // some (key > row) pairs in this tile
-#pragma unroll
-            for (int c = 0; c < 64; c += 4) {
-                const float4 l4 = *reinterpret_cast<const float4 *>(Ls + c);
-                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float v = ex2_approx(__uint_as_float(sr[c + e]) * scale_log2 - lv[e]);
-                    if (diag && key > i0 + c + e) v = 0.0f;
-                    p[c + e] = v;
-                }
-            }
+            uint64_t pp[32];              // P pairs (fp32) kept for dS
             {
                 uint32_t pk[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
+                for (int c = 0; c < 64; c += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4 *>(Ls + c);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int cc = c + 2 * h;
+                        const float2 a = f2_unpack(ffma2(f2_pack(__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])), cs2,
+                                                         h == 0 ? f2_pack(l4.x, l4.y) : f2_pack(l4.z, l4.w)));
+                        float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
+                        if (diag) {
+                            if (key > i0 + cc) p0 = 0.0f;
+                            if (key > i0 + cc + 1) p1 = 0.0f;
+                        }
+                        pp[cc / 2] = f2_pack(p0, p1);
+                        pk[cc / 2] = pack_bf16x2(p0, p1);
+                    }
+                }
                 tmem_st32(tmem + lane_off + C::COL_S + 64 * b, pk);
                 tmem_wait_st();
             }
             tc_fence_before_sync();
-            mbar_arrive(&bars->p_full[b]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->p_full[b]);
 
             if (!(ok = warp_wait(&bars->dp_full, it & 1, bars, status))) break;
             tc_fence_after_sync();
             if (it >= 2 && !(ok = warp_wait(&bars->ds_empty[b], ph2 ^ 1, bars, status))) break;
             uint8_t *dsrow = smem + C::OFF_DS + b * C::DS_BYTES + r * 128;
+            // dS = P (dP - D) scale on packed pairs
+            const uint64_t sc2 = f2_pack(scale, scale);
+            const uint64_t m1 = f2_pack(-1.0f, -1.0f);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t dp[32];
@@ -336,9 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int c = 32 * h + 2 * e;
-                    const float d0 = p[c] * (__uint_as_float(dp[2 * e]) - Ds[c]) * scale;
-                    const float d1 = p[c + 1] * (__uint_as_float(dp[2 * e + 1]) - Ds[c + 1]) * scale;
-                    pk[e] = pack_bf16x2(d0, d1);
+                    const float2 d2 = *reinterpret_cast<const float2 *>(Ds + c);
+                    const uint64_t t = ffma2(f2_pack(d2.x, d2.y), m1, f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])));
+                    const float2 ds = f2_unpack(fmul2(fmul2(pp[c / 2], sc2), t));
+                    pk[e] = pack_bf16x2(ds.x, ds.y);
                 }
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
@@ -353,7 +364,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
-            mbar_arrive(&bars->ds_full[b]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->ds_full[b]);
         }
         // epilogue: dV rows
         if (ok && warp_wait(&bars->done, 0, bars, status)) {
@@ -395,7 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 reg_fence32(g);
                 reg_fence32(g + 32);
                 tc_fence_before_sync();
-                mbar_arrive(&bars->dq_empty);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->dq_empty);
                 const int i0 = (it0 + it) * BM;
                 const int rows = min(BM, S - i0);
                 // the staging tile is free once the previous bulk reduce has read it

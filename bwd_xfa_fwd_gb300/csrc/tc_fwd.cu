@@ -60,7 +60,7 @@ struct Bars {
     uint64_t q_full;
     uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
     uint64_t s_full[2];   // S_t ready in TMEM (tensor-core commit)
-    uint64_t p_full[2];   // P_t written to TMEM (128 softmax threads)
+    uint64_t p_full[2];   // P_t written to TMEM (one arrival per softmax warp)
     uint64_t o_full[2];   // O_t complete (commit after the last P.V)
     uint64_t drain;       // MMA drain at teardown
     uint32_t tmem_base;
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&bars->s_full[t], 1);
-            mbar_init(&bars->p_full[t], BM);
+            mbar_init(&bars->p_full[t], BM / 32);   // one arrival per softmax warp
             mbar_init(&bars->o_full[t], 1);
         }
         mbar_init(&bars->drain, 1);
@@ -286,16 +286,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 128; ++c)
                     if (c > r) sr[c] = 0xff800000u;   // -inf
             }
-            // row max with 8 independent partial maxima (short dependency chains)
-            float mx8[8];
+            // row max: 4 independent chains of 3-input maxima
+            float mx4[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) mx8[e] = __uint_as_float(sr[e]);
+            for (int e = 0; e < 4; ++e) mx4[e] = __uint_as_float(sr[e]);
 #pragma unroll
-            for (int c = 8; c < 128; c += 8)
+            for (int c = 4; c < 128; c += 8)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], __uint_as_float(sr[c + e]));
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                for (int e = 0; e < 4; ++e)
+                    mx4[e] = fmax3(mx4[e], __uint_as_float(sr[c + 2 * e]), __uint_as_float(sr[c + 2 * e + 1]));
+            const float mx = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
             const float m_new = fmaxf(m, mx * scale_log2);   // scale > 0: max commutes with the scaling
             const bool need = m_new > m + kRescaleThreshold;
             if (__any_sync(0xffffffffu, need)) {
@@ -316,29 +316,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 m = m_new;
             }
-            // p = 2^(s * scale * log2(e) - m): one FFMA + one ex2 per score; 8 partial row sums
-            const float neg_m = -m;
-            float l8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) l8[e] = 0.0f;
+            // p = 2^(s * scale * log2(e) - m): packed FFMA pairs + ex2; 4 packed partial row sums
+            const uint64_t c2 = f2_pack(scale_log2, scale_log2);
+            const uint64_t nm2 = f2_pack(-m, -m);
+            uint64_t l2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int c = 64 * h + 2 * e;
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), scale_log2, neg_m));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), scale_log2, neg_m));
-                    l8[(2 * e) & 7] += p0;
-                    l8[(2 * e + 1) & 7] += p1;
+                    const float2 a = f2_unpack(ffma2(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, nm2));
+                    const float p0 = ex2_approx(a.x);
+                    const float p1 = ex2_approx(a.y);
+                    l2[e & 3] = fadd2(l2[e & 3], f2_pack(p0, p1));
                     pk[e] = pack_bf16x2(p0, p1);
                 }
                 tmem_st32(tS + 32 * h, pk);
             }
-            l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+            {
+                const float2 a = f2_unpack(fadd2(fadd2(l2[0], l2[1]), fadd2(l2[2], l2[3])));
+                l += a.x + a.y;
+            }
             tmem_wait_st();
             tc_fence_before_sync();
-            mbar_arrive(&bars->p_full[t]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->p_full[t]);
         }
         if (ok && n_mine > 0 && warp_wait(&bars->o_full[t], 0, bars, status)) {
             tc_fence_after_sync();

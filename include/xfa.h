@@ -84,7 +84,7 @@ int xfa_fwd_impl(const void *q, const void *k, const void *v, void *out, float *
 
 /*
  * Bytes of device workspace xfa_bwd needs for this shape (a pure function of
- * its arguments; 0 for invalid arguments).  Holds D [bh][S'] and L*log2(e)
+ * its arguments; 0 for invalid arguments).  Holds D [bh][S'] and -L*log2(e)
  * [bh][S'] fp32 (S' = S rounded up to 128) and, for bf16, an fp32 dQ
  * accumulator [bh][S][hd].
  */
@@ -121,8 +121,8 @@ int xfa_bwd_impl(const void *q, const void *k, const void *v, const void *out, c
  * The three stages of xfa_bwd as separate calls, for callers that schedule
  * (or time) them individually.  xfa_bwd_impl is exactly prep, main, finish
  * in this order on one stream, with the same arguments and workspace.
- *   prep   : D_i = dO_i . O_i and L_i * log2(e) into the workspace (padded
- *            rows: D = 0, L = +inf), and clears the fp32 dQ accumulator (the
+ *   prep   : D_i = dO_i . O_i and -L_i * log2(e) into the workspace (padded
+ *            rows: D = 0, -L*log2(e) = -inf), and clears the fp32 dQ accumulator (the
  *            workspace for bf16, dq itself for fp32).
  *   main   : the backward kernel (dK, dV written; dQ summed into the accumulator).
  *   finish : dQ accumulator -> dq in the output dtype (nothing to do for fp32).
