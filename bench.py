@@ -100,8 +100,11 @@ def make_device_inputs(w, torch):
     x = inputs.workload_inputs(w)
     dev = {}
     for n in ("q", "k", "v", "dout"):
-        bits = torch.from_numpy(np.ascontiguousarray(x[n].stored).view(np.int16))
-        dev[n] = bits.view(torch.bfloat16).cuda()
+        if w.dtype == "f32":
+            dev[n] = torch.from_numpy(np.ascontiguousarray(x[n].stored)).cuda()
+        else:
+            bits = torch.from_numpy(np.ascontiguousarray(x[n].stored).view(np.int16))
+            dev[n] = bits.view(torch.bfloat16).cuda()
     return x, dev
 
 
@@ -212,35 +215,39 @@ def run_ours(args, w):
 
     # end to end through the C ABI with host buffers: pinned H2D of the step's
     # inputs, forward + backward, D2H of O, L, dQ, dK, dV
-    host_in = {n: t.cpu().pin_memory() for n, t in dev.items()}
-    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (out, lse) + grads]
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e2e = None
+    if not args.no_e2e:
+        host_in = {n: t.cpu().pin_memory() for n, t in dev.items()}
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (out, lse) + grads]
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
 
-    def e2e_step():
-        for n in ("q", "k", "v", "dout"):
-            dev[n].copy_(host_in[n], non_blocking=True)
-        binding.fwd(q, k, v, w.scale, out=out, lse=lse)
-        binding.bwd(q, k, v, out, do, lse, w.scale, workspace=ws, grads=grads)
-        for h, d in zip(host_out, (out, lse) + grads):
-            h.copy_(d, non_blocking=True)
+        def e2e_step():
+            for n in ("q", "k", "v", "dout"):
+                dev[n].copy_(host_in[n], non_blocking=True)
+            binding.fwd(q, k, v, w.scale, out=out, lse=lse)
+            binding.bwd(q, k, v, out, do, lse, w.scale, workspace=ws, grads=grads)
+            for h, d in zip(host_out, (out, lse) + grads):
+                h.copy_(d, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    ke = max(3, K // 4)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(ke):
-        e2e_step()
-    b.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = a.elapsed_time(b) / ke
-    e2e_val = (f_fwd + f_bwd) * world / (e2e_ms * 1e-3) / 1e12
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        ke = max(3, K // 4)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / ke
+        e2e = {"value": (f_fwd + f_bwd) * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     pk, pk_kind = peaks()
     peak_tc = float(pk["bf16_tflops"])
     main_tflops = f_bwd / (per["main"] * 1e-3) / 1e12
+    fam = f"tc_{{}}_kernel<{w.hd}>" if w.dtype == "bf16" else f"simt_{{}}_kernel<{w.dtype},{w.hd}>"
     prep_bytes = w.bh * w.S * (2 * w.hd * 2 + 4 + 4 + 4 + 4 * w.hd)
     line = {
         "metric": METRIC,
@@ -253,7 +260,7 @@ def run_ours(args, w):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": w.dtype,
         "data": "synthetic (seeded N(0,1), bf16-rounded; recipe in bwd_xfa_fwd_gb300/inputs.py)",
         "config": workload_config(w),
         "fwd_tflops": f_fwd / (per["fwd"] * 1e-3) / 1e12,
@@ -263,18 +270,17 @@ def run_ours(args, w):
         "peak_bf16_tflops": peak_tc,
         "peak_kind": f"{pk_kind} burst bf16 dense (cuBLAS)",
         "stage_ms": per,
-        "roofline": {"kernel": "tc_bwd_kernel<128> (xfa_bwd_main)", "bound": "tensor", "achieved": main_tflops,
+        "roofline": {"kernel": fam.format("bwd") + " (xfa_bwd_main)", "bound": "tensor", "achieved": main_tflops,
                      "peak": peak_tc, "unit": "TFLOP/s", "frac": main_tflops / peak_tc, "traffic": None,
                      "peak_source": f"{pk_kind} bf16_tflops"},
-        "roofline_fwd": {"kernel": "tc_fwd_kernel<128> (xfa_fwd)", "bound": "tensor",
+        "roofline_fwd": {"kernel": fam.format("fwd") + " (xfa_fwd)", "bound": "tensor",
                          "achieved": f_fwd / (per["fwd"] * 1e-3) / 1e12, "peak": peak_tc, "unit": "TFLOP/s",
                          "frac": f_fwd / (per["fwd"] * 1e-3) / 1e12 / peak_tc, "traffic": None},
         "roofline_prep": {"kernel": "rowdot_kernel (xfa_bwd_prep)", "bound": "hbm",
                           "achieved": prep_bytes / (per["prep"] * 1e-3) / 1e9, "peak": float(pk["hbm_gbs"]),
                           "unit": "GB/s", "frac": prep_bytes / (per["prep"] * 1e-3) / 1e9 / float(pk["hbm_gbs"]),
                           "traffic": None},
-        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
+        "e2e": e2e,
         "gpu_launches": 4 * K,
         "clocks": clk.result,
     }
@@ -295,10 +301,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=sorted(inputs.WORKLOADS),
+                    help="workload id (default: the S=8192 benchmark workload; others for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    w = inputs.WORKLOADS[WORKLOAD_ID]
+    w = inputs.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -43,6 +43,7 @@ template <int HD>
 constexpr int ring_depth() { return HD == 128 ? 3 : 4; }   // query-tile (Q, dO, L, D) ring stages
 constexpr int kThreads = 320;
 constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr int kHeadBundle = 4;   // heads scheduled together (L2 reuse of inputs and dQ accumulator)
 
 template <int HD>
 struct Cfg {
@@ -124,8 +125,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *dq_stage = reinterpret_cast<float *>(smem + C::OFF_DQ);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    const int jt = (int)(blockIdx.x / bh);        // key tile: low tiles have the most work, go first
-    const int head = (int)(blockIdx.x % bh);
+    // Work order: heads in bundles of kHeadBundle (so the inputs and the dQ accumulator of the
+    // heads in flight stay in L2), and within a bundle the key tiles with the most query tiles first.
+    const int nkt = (S + BN - 1) / BN;
+    const int bundle = (int)blockIdx.x / (nkt * kHeadBundle);
+    const int g = min(kHeadBundle, bh - bundle * kHeadBundle);
+    const int idx = (int)blockIdx.x - bundle * nkt * kHeadBundle;
+    const int jt = idx / g;
+    const int head = bundle * kHeadBundle + idx % g;
     const int j0 = jt * BN;
     const int nq_total = (S + BM - 1) / BM;
     const int it0 = (j0 / BM);                    // first query tile at or below the diagonal

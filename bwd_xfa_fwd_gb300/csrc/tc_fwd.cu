@@ -38,6 +38,7 @@ constexpr int kThreads = 320;         // 10 warps
 constexpr int kWarpTma = 8, kWarpMma = 9;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+constexpr int kHeadBundle = 8;              // heads scheduled together (L2 reuse of K/V)
 
 template <int HD>
 struct Cfg {
@@ -117,9 +118,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     Bars *bars = reinterpret_cast<Bars *>(smem + C::OFF_BAR);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
+    // Work order: heads in bundles of kHeadBundle (so the K/V of the heads in flight stay in
+    // L2), and within a bundle the heaviest (longest) query blocks first.
     const int nqb = (S + 2 * BM - 1) / (2 * BM);
-    const int qb = nqb - 1 - (int)(blockIdx.x / bh);   // heaviest query blocks first
-    const int head = (int)(blockIdx.x % bh);
+    const int bundle = (int)blockIdx.x / (nqb * kHeadBundle);
+    const int g = min(kHeadBundle, bh - bundle * kHeadBundle);   // heads in this bundle
+    const int idx = (int)blockIdx.x - bundle * nqb * kHeadBundle;
+    const int qb = nqb - 1 - idx / g;
+    const int head = bundle * kHeadBundle + idx % g;
     const int q0 = qb * 2 * BM;
     const bool t1 = q0 + BM < S;
     const int n_t0 = 2 * qb + 1, n_t1 = t1 ? 2 * qb + 2 : 0;   // key tiles per query tile
