@@ -13,19 +13,20 @@
 //   * warp 8 streams Q_i, dO_i (TMA, 128-byte swizzle) with -L_i*log2(e) and
 //     D_i (bulk copies) through a ring;
 //   * warp 9 (one thread) issues, per query tile:
-//       S^T  = K_j Q_i^T            (M=128 keys, N=64 rows, K=hd)  -> TMEM, double buffered
+//       S^T  = K_j Q_i^T            (M=128 keys, N=64 rows, K=hd; A = K_j kept in TMEM)
 //       dP^T = V_j dO_i^T           (M=128, N=64, K=hd)            -> TMEM
 //       dV  += P^T dO_i             (A = P^T bf16 in TMEM, B = dO_i MN-major)
-//       dK  += dS^T Q_i             (A = dS^T in smem, B = Q_i MN-major)
-//       dQ^T = K_j^T dS^T           (M=hd, N=64, K=128 keys)       -> TMEM
+//       dK  += dS^T Q_i             (A = dS^T bf16 in TMEM, B = Q_i MN-major)
+//       dQ^T = K_j^T dS^T           (M=hd, N=64, K=128 keys; B = dS^T in smem) -> TMEM
+//     Operands kept in TMEM spare shared-memory bandwidth, which bounds this kernel;
 //   * warps 0-3 (thread = key) turn S^T, dP^T into P^T (bf16, back into the
 //     S^T columns) and dS^T (bf16, swizzled smem);
 //   * warps 4-7 (thread = hd index) read dQ^T from TMEM, stage it as a
 //     row-major fp32 [64][hd] tile in shared memory (one contiguous block of
 //     the [S][hd] accumulator) and add it into global memory with a single
 //     TMA bulk reduce-add; a conversion kernel writes dQ afterwards.
-// TMEM map (512 columns): dK [0,hd) dV [hd,2hd) S^T x2 [2hd,2hd+128)
-//                         dP^T [2hd+128,2hd+192) dQ^T [2hd+192,2hd+256).
+// TMEM map (512 columns): dK [0,hd) dV [hd,2hd) S^T [2hd,2hd+64) dP^T [2hd+64,2hd+128)
+//                         dQ^T [2hd+128,2hd+192) K_j [2hd+192,2hd+192+hd/2).
 // For hd = 64 the dQ^T MMA still runs with M = 128; lanes 64-127 hold
 // products of V and are never read.
 #include <cuda_bf16.h>
@@ -63,8 +64,10 @@ struct Cfg {
     static constexpr int OFF_LD = OFF_DQ + BM * HD * 4;   // per stage: Lg[64], D[64]
     static constexpr int OFF_BAR = OFF_LD + NSQ * 2 * BM * 4;
     static constexpr int SMEM = OFF_BAR + 256 + 1024;   // barriers + alignment slack
-    static constexpr uint32_t COL_DK = 0, COL_DV = HD, COL_S = 2 * HD, COL_DP = 2 * HD + 128,
-                              COL_DQ = 2 * HD + 192;
+    // TMEM columns: dK, dV accumulators; S^T (P^T bf16 written back into its first 32 columns);
+    // dP^T (dS^T bf16 written back into its first 32 columns); dQ^T; K_j as a bf16 A operand.
+    static constexpr uint32_t COL_DK = 0, COL_DV = HD, COL_S = 2 * HD, COL_DP = 2 * HD + 64,
+                              COL_DQ = 2 * HD + 128, COL_KT = 2 * HD + 192;
     static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -73,8 +76,8 @@ constexpr int kMaxRing = 4;
 struct Bars {
     uint64_t kv_full;
     uint64_t q_full[kMaxRing], q_empty[kMaxRing];
-    uint64_t s_full[2], p_full[2], ds_full[2], ds_empty[2];
-    uint64_t dp_full, dq_full, dq_empty, done, drain;
+    uint64_t s_full, p_full, ds_full[2], ds_empty[2];
+    uint64_t kt_full, dp_full, dq_full, dq_empty, done, drain;
     uint32_t tmem_base;
     int abort;
 };
@@ -105,6 +108,16 @@ __device__ __forceinline__ void issue_rows_dot(uint32_t d_tmem, uint64_t a_desc,
         mma_ss(d_tmem, sdesc_advance(a_desc, (ks / 4) * Cfg<HD>::KV_SUB + k_off),
                sdesc_advance(b_desc, (ks / 4) * Cfg<HD>::Q_SUB + k_off), idesc, ks > 0);
     }
+}
+
+// S^T[M=128 keys, N=64 rows] = K_j (A: bf16 pairs in TMEM, hd along the columns) * Q_i^T (B: K-major smem).
+template <int HD>
+__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t k_tmem, uint64_t q_desc, uint32_t idesc)
+{
+#pragma unroll
+    for (int ks = 0; ks < HD / 16; ++ks)
+        mma_ts(d_tmem, k_tmem + ks * 8, sdesc_advance(q_desc, (ks / 4) * Cfg<HD>::Q_SUB + (ks % 4) * 32), idesc,
+               ks > 0 ? 1u : 0u);
 }
 
 template <int HD>
@@ -145,11 +158,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->q_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&bars->s_full[b], 1);
-            mbar_init(&bars->p_full[b], 4);    // one arrival per key warp
-            mbar_init(&bars->ds_full[b], 4);
+            mbar_init(&bars->ds_full[b], 4);   // one arrival per key warp
             mbar_init(&bars->ds_empty[b], 1);
         }
+        mbar_init(&bars->s_full, 1);
+        mbar_init(&bars->p_full, 4);
+        mbar_init(&bars->kt_full, 4);
         mbar_init(&bars->dp_full, 1);
         mbar_init(&bars->dq_full, 1);
         mbar_init(&bars->dq_empty, HD / 32);   // one arrival per readout warp
@@ -209,21 +223,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t k_s = smem_u32(smem + C::OFF_K), v_s = smem_u32(smem + C::OFF_V);
         const uint32_t q_s = smem_u32(smem + C::OFF_Q), do_s = smem_u32(smem + C::OFF_DO);
         const uint32_t ds_s = smem_u32(smem + C::OFF_DS);
-        // K-major views (hd contiguous) for S^T = K Q^T and dP^T = V dO^T
-        const uint64_t k_km = sdesc_sw128(k_s, 16, 1024), v_km = sdesc_sw128(v_s, 16, 1024);
+        // K-major views (hd contiguous) for dP^T = V dO^T and the B operand Q_i of S^T
+        const uint64_t v_km = sdesc_sw128(v_s, 16, 1024);
         const uint64_t q_km = sdesc_sw128(q_s, 16, 1024), do_km = sdesc_sw128(do_s, 16, 1024);
         // MN-major views: B = dO_i / Q_i for dV / dK, A = K_j^T for dQ^T; dS^T as K-major A / MN-major B
         const uint64_t do_mn = sdesc_sw128(do_s, C::Q_SUB, 1024), q_mn = sdesc_sw128(q_s, C::Q_SUB, 1024);
         const uint64_t k_mn = sdesc_sw128(k_s, C::KV_SUB, 1024);
-        const uint64_t ds_km = sdesc_sw128(ds_s, 16, 1024), ds_mn = sdesc_sw128(ds_s, C::DS_BYTES, 1024);
+        const uint64_t ds_mn = sdesc_sw128(ds_s, C::DS_BYTES, 1024);
         constexpr uint32_t idesc_acc = idesc_bf16(BN, HD, false, true);    // dV, dK: B MN-major
         constexpr uint32_t idesc_dq = idesc_bf16(128, BM, true, true);     // dQ^T: A, B MN-major
-        bool ok = warp_wait(&bars->kv_full, 0, bars, status) && warp_wait(&bars->q_full[0], 0, bars, status);
+        constexpr uint32_t idesc_s = idesc_bf16(BN, BM, false, false);     // S^T: A = K_j from TMEM
+        bool ok = warp_wait(&bars->kv_full, 0, bars, status) && warp_wait(&bars->kt_full, 0, bars, status) &&
+                  warp_wait(&bars->q_full[0], 0, bars, status);
         if (ok) {
             tc_fence_after_sync();
             if (leader) {
-                issue_rows_dot<HD>(tmem + C::COL_S, k_km, q_km);
-                tc_commit(&bars->s_full[0]);
+                issue_s<HD>(tmem + C::COL_S, tmem + C::COL_KT, q_km, idesc_s);
+                tc_commit(&bars->s_full);
                 issue_rows_dot<HD>(tmem + C::COL_DP, v_km, do_km);
                 tc_commit(&bars->dp_full);
             }
@@ -234,38 +250,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ph2 = (it >> 1) & 1;
             const uint32_t qoff = st * C::Q_BYTES, dsoff = b * C::DS_BYTES;
             const int nx = it + 1, stn = nx % NSQ;
-            if (nx < n) {   // S^T of the next tile into the other buffer (its P was consumed in order)
-                if (!(ok = warp_wait(&bars->q_full[stn], (nx / NSQ) & 1, bars, status))) break;
-                tc_fence_after_sync();
-                if (leader) {
-                    issue_rows_dot<HD>(tmem + C::COL_S + 64 * (nx & 1), k_km, sdesc_advance(q_km, stn * C::Q_BYTES));
-                    tc_commit(&bars->s_full[nx & 1]);
-                }
-                __syncwarp();
-            }
-            // dV += P^T dO_i  (P^T: bf16 in the S^T columns of buffer b)
-            if (!(ok = warp_wait(&bars->p_full[b], ph2, bars, status))) break;
+            // dV += P^T dO_i  (P^T: bf16 in the first columns of S^T)
+            if (!(ok = warp_wait(&bars->p_full, it & 1, bars, status))) break;
             tc_fence_after_sync();
             if (leader) {
 #pragma unroll
                 for (int ks = 0; ks < BM / 16; ++ks)
-                    mma_ts(tmem + C::COL_DV, tmem + C::COL_S + 64 * b + ks * 8,
-                           sdesc_advance(do_mn, qoff + ks * 2048), idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
+                    mma_ts(tmem + C::COL_DV, tmem + C::COL_S + ks * 8, sdesc_advance(do_mn, qoff + ks * 2048), idesc_acc,
+                           (it > 0 || ks > 0) ? 1u : 0u);
             }
             __syncwarp();
-            // dS^T is in smem and dP^T has been read: next dP^T first, then dK and dQ^T
+            if (nx < n) {   // next S^T: its columns are free once the dV MMA above has read P^T (in order)
+                if (!(ok = warp_wait(&bars->q_full[stn], (nx / NSQ) & 1, bars, status))) break;
+                tc_fence_after_sync();
+                if (leader) {
+                    issue_s<HD>(tmem + C::COL_S, tmem + C::COL_KT, sdesc_advance(q_km, stn * C::Q_BYTES), idesc_s);
+                    tc_commit(&bars->s_full);
+                }
+                __syncwarp();
+            }
+            // dS^T is in TMEM (first columns of dP^T) and in smem: dK first (reads the TMEM copy),
+            // then the next dP^T may overwrite those columns
             if (!(ok = warp_wait(&bars->ds_full[b], ph2, bars, status))) break;
             tc_fence_after_sync();
             if (leader) {
+#pragma unroll
+                for (int ks = 0; ks < BM / 16; ++ks)
+                    mma_ts(tmem + C::COL_DK, tmem + C::COL_DP + ks * 8, sdesc_advance(q_mn, qoff + ks * 2048), idesc_acc,
+                           (it > 0 || ks > 0) ? 1u : 0u);
+                tc_commit(&bars->q_empty[st]);
                 if (nx < n) {
                     issue_rows_dot<HD>(tmem + C::COL_DP, v_km, sdesc_advance(do_km, stn * C::Q_BYTES));
                     tc_commit(&bars->dp_full);
                 }
-#pragma unroll
-                for (int ks = 0; ks < BM / 16; ++ks)
-                    mma_ss(tmem + C::COL_DK, sdesc_advance(ds_km, dsoff + ks * 32), sdesc_advance(q_mn, qoff + ks * 2048),
-                           idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
-                tc_commit(&bars->q_empty[st]);
             }
             __syncwarp();
             if (it > 0 && !(ok = warp_wait(&bars->dq_empty, (it - 1) & 1, bars, status))) break;
@@ -291,18 +308,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = warp * 32 + lane;
         const int key = j0 + r;
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        bool ok = true;
-        for (int it = 0; it < n; ++it) {
+        // K_j row r -> TMEM (bf16 pairs along hd) as the A operand of S^T = K_j Q_i^T
+        bool ok = warp_wait(&bars->kv_full, 0, bars, status);
+        if (ok) {
+#pragma unroll
+            for (int sub = 0; sub < C::SUB; ++sub) {
+                uint32_t kw[32];
+                const uint8_t *krow = smem + C::OFF_K + sub * C::KV_SUB + r * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v4 = *reinterpret_cast<const uint4 *>(krow + ((c ^ (r & 7)) << 4));
+                    kw[4 * c + 0] = v4.x;
+                    kw[4 * c + 1] = v4.y;
+                    kw[4 * c + 2] = v4.z;
+                    kw[4 * c + 3] = v4.w;
+                }
+                tmem_st32(tmem + lane_off + C::COL_KT + 32 * sub, kw);
+            }
+            tmem_wait_st();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->kt_full);
+        }
+        for (int it = 0; ok && it < n; ++it) {
             const int b = it & 1, st = it % NSQ;
             const uint32_t ph2 = (it >> 1) & 1;
             const int i0 = (it0 + it) * BM;
             const float *Ls = ld_s + st * 2 * BM;
             const float *Ds = Ls + BM;
-            if (!(ok = warp_wait(&bars->s_full[b], ph2, bars, status))) break;
+            if (!(ok = warp_wait(&bars->s_full, it & 1, bars, status))) break;
             tc_fence_after_sync();
             uint32_t sr[64];
-            tmem_ld32(tmem + lane_off + C::COL_S + 64 * b, sr);
-            tmem_ld32(tmem + lane_off + C::COL_S + 64 * b + 32, sr + 32);
+            tmem_ld32(tmem + lane_off + C::COL_S, sr);
+            tmem_ld32(tmem + lane_off + C::COL_S + 32, sr + 32);
             tmem_wait_ld();
             reg_fence32(sr);
             reg_fence32(sr + 32);
@@ -329,12 +367,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pk[cc / 2] = pack_bf16x2(p0, p1);
                     }
                 }
-                tmem_st32(tmem + lane_off + C::COL_S + 64 * b, pk);
+                tmem_st32(tmem + lane_off + C::COL_S, pk);
                 tmem_wait_st();
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->p_full[b]);
+            if (lane == 0) mbar_arrive(&bars->p_full);
 
             if (!(ok = warp_wait(&bars->dp_full, it & 1, bars, status))) break;
             tc_fence_after_sync();
@@ -358,6 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float2 ds = f2_unpack(fmul2(fmul2(pp[c / 2], sc2), t));
                     pk[e] = pack_bf16x2(ds.x, ds.y);
                 }
+                // dS^T pairs into the dP^T columns already read (A operand of dK += dS^T Q_i)
+                tmem_st16(tmem + lane_off + C::COL_DP + 16 * h, pk);
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     const int chunk = 4 * h + v;                   // 16-byte chunk of the 128-byte row
@@ -369,6 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint4 *>(dsrow + ((chunk ^ (r & 7)) << 4)) = w;
                 }
             }
+            tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before_sync();
             __syncwarp();
