@@ -32,6 +32,7 @@ sys.path.insert(0, ROOT)
 from bwd_xfa_fwd_gb300 import inputs  # noqa: E402
 
 METRIC = "causal attn fwd / bwd TFLOP/s at 1 GB300 and fraction of bf16 tensor peak"
+FAMILIES = {"auto": 0, "simt": 1, "tcgen05": 2, "tcgen05_det": 3}   # xfa_impl codes
 WORKLOAD_ID = 5
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -186,6 +187,7 @@ def run_ours(args, w):
     ws = torch.empty(binding.workspace_bytes(w.bh, w.S, w.hd, q.dtype), device="cuda", dtype=torch.uint8)
     stream = torch.cuda.current_stream()
 
+    impl = FAMILIES[args.family]
     stages = ("fwd", "prep", "main", "finish")
     K = args.steps
     ev = {s: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
@@ -209,9 +211,9 @@ def run_ours(args, w):
                 mark("finish", 1)
 
         mark("fwd", 0)
-        binding.fwd(q, k, v, w.scale, out=out, lse=lse)
+        binding.fwd(q, k, v, w.scale, impl, out=out, lse=lse)
         mark("fwd", 1)
-        binding.bwd_stages(q, k, v, out, do, lse, w.scale, ws, grads, hook=hook)
+        binding.bwd_stages(q, k, v, out, do, lse, w.scale, ws, grads, impl=impl, hook=hook)
 
     for _ in range(args.warmup):
         step()
@@ -255,8 +257,8 @@ def run_ours(args, w):
         def e2e_step():
             for n in ("q", "k", "v", "dout"):
                 dev[n].copy_(host_in[n], non_blocking=True)
-            binding.fwd(q, k, v, w.scale, out=out, lse=lse)
-            binding.bwd(q, k, v, out, do, lse, w.scale, workspace=ws, grads=grads)
+            binding.fwd(q, k, v, w.scale, impl, out=out, lse=lse)
+            binding.bwd(q, k, v, out, do, lse, w.scale, impl, workspace=ws, grads=grads)
             for h, d in zip(host_out, (out, lse) + grads):
                 h.copy_(d, non_blocking=True)
 
@@ -292,7 +294,7 @@ def run_ours(args, w):
         "vs_baseline": None,
         "dtype": w.dtype,
         "data": "synthetic (seeded N(0,1), bf16-rounded; recipe in bwd_xfa_fwd_gb300/inputs.py)",
-        "config": workload_config(w),
+        "config": dict(workload_config(w), kernel_family=args.family),
         "fwd_tflops": f_fwd / (per["fwd"] * 1e-3) / 1e12,
         "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
         "fwd_frac_of_peak": f_fwd / (per["fwd"] * 1e-3) / 1e12 / peak_tc,
@@ -334,6 +336,9 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--family", choices=sorted(FAMILIES), default="auto",
+                    help="kernel family (xfa_impl): auto, tcgen05 (dQ by fp32 reductions), "
+                         "tcgen05_det (dQ by a separate pass, bit-reproducible), simt")
     ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=sorted(inputs.WORKLOADS),
                     help="workload id (default: the S=8192 benchmark workload; others for profiling)")
     args = ap.parse_args()

@@ -15,7 +15,7 @@ import torch
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libxfa.so")
 
 XFA_F32, XFA_BF16 = 0, 1
-IMPL_AUTO, IMPL_SIMT, IMPL_TCGEN05 = 0, 1, 2
+IMPL_AUTO, IMPL_SIMT, IMPL_TCGEN05, IMPL_TCGEN05_DET = 0, 1, 2, 3
 XFA_OK, XFA_ERR_INVALID_ARG, XFA_ERR_UNSUPPORTED, XFA_ERR_TIMEOUT, XFA_ERR_WORKSPACE, XFA_ERR_DEVICE = range(6)
 XFA_ERR_CUDA_BASE = 1000
 
@@ -44,9 +44,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "xfa_bwd_workspace_bytes": ([i, i, i, i], sz),
         "xfa_bwd": ([vp] * 9 + [i, i, i, f, i, vp, sz, vp], i),
         "xfa_bwd_impl": ([vp] * 9 + [i, i, i, f, i, vp, sz, i, vp], i),
-        "xfa_bwd_prep": ([vp, vp, vp, vp, i, i, i, i, vp, sz, vp], i),
+        "xfa_bwd_prep": ([vp, vp, vp, vp, i, i, i, i, vp, sz, i, vp], i),
         "xfa_bwd_main": ([vp] * 7 + [i, i, i, f, i, vp, sz, i, vp], i),
-        "xfa_bwd_finish": ([vp, i, i, i, i, vp, sz, vp], i),
+        "xfa_bwd_finish": ([vp, i, i, i, i, vp, sz, i, vp], i),
         "xfa_rowdot": ([vp, vp, vp, i, i, i, i, vp], i),
         "xfa_accumulate": ([vp, vp, sz, i, vp], i),
         "xfa_status": ([vp], i),
@@ -143,12 +143,12 @@ def bwd_stages(q, k, v, out, dout, lse, scale, workspace, grads, impl: int = IMP
     lib, st, ws, nws = load(), _stream(q), _p(workspace), workspace.numel()
     hook = hook or (lambda name: None)
     hook("prep")
-    _check(lib.xfa_bwd_prep(_p(out), _p(dout), _p(lse), _p(dq), bh, S, hd, dt, ws, nws, st), "xfa_bwd_prep")
+    _check(lib.xfa_bwd_prep(_p(out), _p(dout), _p(lse), _p(dq), bh, S, hd, dt, ws, nws, impl, st), "xfa_bwd_prep")
     hook("main")
     _check(lib.xfa_bwd_main(_p(q), _p(k), _p(v), _p(dout), _p(dq), _p(dk), _p(dv), bh, S, hd, float(scale), dt, ws,
                             nws, impl, st), "xfa_bwd_main")
     hook("finish")
-    _check(lib.xfa_bwd_finish(_p(dq), bh, S, hd, dt, ws, nws, st), "xfa_bwd_finish")
+    _check(lib.xfa_bwd_finish(_p(dq), bh, S, hd, dt, ws, nws, impl, st), "xfa_bwd_finish")
     hook("end")
     return dq, dk, dv
 

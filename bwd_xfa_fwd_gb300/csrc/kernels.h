@@ -55,7 +55,10 @@ cudaError_t launch_selftest_timeout(unsigned timeout_us, int *status, cudaStream
 
 // tcgen05 family: bf16, hd in {64, 128}.  Return an XFA_* code.
 int launch_tc_fwd(const FwdParams &p, cudaStream_t st);
-int launch_tc_bwd(const BwdParams &p, cudaStream_t st);
+// Key-tile backward: dK, dV and, when fused_dq, dQ summed into p.dq_acc.
+int launch_tc_bwd(const BwdParams &p, cudaStream_t st, bool fused_dq);
+// Query-tile dQ pass: writes p.dq (bf16) directly, no atomics.
+int launch_tc_dq(const BwdParams &p, cudaStream_t st);
 
 // Encodes the TMA descriptors; resolved once from the driver (xfa_api.cu).
 int encode_tmap_bf16_3d(void *tmap, const void *base, int hd, int S, int bh, int box_rows);

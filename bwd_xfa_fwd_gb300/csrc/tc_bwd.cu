@@ -120,7 +120,9 @@ __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t k_tmem, uint64
                ks > 0 ? 1u : 0u);
 }
 
-template <int HD>
+// FUSED_DQ: dQ^T is formed here and summed into the fp32 accumulator (bulk reduce-add);
+// otherwise dQ is left to the query-tile pass (tc_dq.cu) and this kernel does dK, dV only.
+template <int HD, bool FUSED_DQ>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -285,17 +287,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             __syncwarp();
-            if (it > 0 && !(ok = warp_wait(&bars->dq_empty, (it - 1) & 1, bars, status))) break;
-            tc_fence_after_sync();
-            if (leader) {
+            if (FUSED_DQ) {
+                if (it > 0 && !(ok = warp_wait(&bars->dq_empty, (it - 1) & 1, bars, status))) break;
+                tc_fence_after_sync();
+                if (leader) {
 #pragma unroll
-                for (int ks = 0; ks < BN / 16; ++ks)
-                    mma_ss(tmem + C::COL_DQ, sdesc_advance(k_mn, ks * 2048), sdesc_advance(ds_mn, dsoff + ks * 2048),
-                           idesc_dq, ks > 0 ? 1u : 0u);
-                tc_commit(&bars->dq_full);
-                tc_commit(&bars->ds_empty[b]);
+                    for (int ks = 0; ks < BN / 16; ++ks)
+                        mma_ss(tmem + C::COL_DQ, sdesc_advance(k_mn, ks * 2048), sdesc_advance(ds_mn, dsoff + ks * 2048),
+                               idesc_dq, ks > 0 ? 1u : 0u);
+                    tc_commit(&bars->dq_full);
+                    tc_commit(&bars->ds_empty[b]);
+                }
+                __syncwarp();
             }
-            __syncwarp();
         }
         if (leader) {
             if (ok) tc_commit(&bars->done);
@@ -376,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             if (!(ok = warp_wait(&bars->dp_full, it & 1, bars, status))) break;
             tc_fence_after_sync();
-            if (it >= 2 && !(ok = warp_wait(&bars->ds_empty[b], ph2 ^ 1, bars, status))) break;
+            if (FUSED_DQ && it >= 2 && !(ok = warp_wait(&bars->ds_empty[b], ph2 ^ 1, bars, status))) break;
             uint8_t *dsrow = smem + C::OFF_DS + b * C::DS_BYTES + r * 128;
             // dS = P (dP - D) scale on packed pairs
             const uint64_t sc2 = f2_pack(scale, scale);
@@ -398,19 +402,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // dS^T pairs into the dP^T columns already read (A operand of dK += dS^T Q_i)
                 tmem_st16(tmem + lane_off + C::COL_DP + 16 * h, pk);
+                if (FUSED_DQ) {
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const int chunk = 4 * h + v;                   // 16-byte chunk of the 128-byte row
-                    uint4 w;
-                    w.x = pk[4 * v + 0];
-                    w.y = pk[4 * v + 1];
-                    w.z = pk[4 * v + 2];
-                    w.w = pk[4 * v + 3];
-                    *reinterpret_cast<uint4 *>(dsrow + ((chunk ^ (r & 7)) << 4)) = w;
+                    for (int v = 0; v < 4; ++v) {
+                        const int chunk = 4 * h + v;                   // 16-byte chunk of the 128-byte row
+                        uint4 w;
+                        w.x = pk[4 * v + 0];
+                        w.y = pk[4 * v + 1];
+                        w.z = pk[4 * v + 2];
+                        w.w = pk[4 * v + 3];
+                        *reinterpret_cast<uint4 *>(dsrow + ((chunk ^ (r & 7)) << 4)) = w;
+                    }
                 }
             }
             tmem_wait_st();
-            fence_proxy_async_smem();
+            if (FUSED_DQ) fence_proxy_async_smem();
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->ds_full[b]);
@@ -444,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int d = wq * 32 + lane;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         bool ok = true;
-        if (d < HD) {
+        if (FUSED_DQ && d < HD) {
             for (int it = 0; it < n; ++it) {
                 if (!(ok = warp_wait(&bars->dq_full, it & 1, bars, status))) break;
                 tc_fence_after_sync();
@@ -507,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int HD>
+template <int HD, bool FUSED_DQ>
 int run(const BwdParams &p, cudaStream_t st)
 {
     alignas(64) CUtensorMap tk, tv, tq, tdo;
@@ -517,7 +523,7 @@ int run(const BwdParams &p, cudaStream_t st)
     if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tdo, p.dout, HD, p.S, p.bh, BM);
     if (rc != XFA_OK) return rc;
     static_assert(Cfg<HD>::SMEM <= 227 * 1024, "shared memory per CTA");
-    auto kern = tc_bwd_kernel<HD>;
+    auto kern = tc_bwd_kernel<HD, FUSED_DQ>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<HD>::SMEM);
     if (e != cudaSuccess) return XFA_ERR_CUDA_BASE + (int)e;
     const int nkt = (p.S + BN - 1) / BN;
@@ -531,11 +537,11 @@ int run(const BwdParams &p, cudaStream_t st)
 
 }  // namespace
 
-int launch_tc_bwd(const BwdParams &p, cudaStream_t st)
+int launch_tc_bwd(const BwdParams &p, cudaStream_t st, bool fused_dq)
 {
     if (p.dtype != XFA_BF16) return XFA_ERR_UNSUPPORTED;
-    if (p.hd == 128) return run<128>(p, st);
-    if (p.hd == 64) return run<64>(p, st);
+    if (p.hd == 128) return fused_dq ? run<128, true>(p, st) : run<128, false>(p, st);
+    if (p.hd == 64) return fused_dq ? run<64, true>(p, st) : run<64, false>(p, st);
     return XFA_ERR_UNSUPPORTED;
 }
 

@@ -82,17 +82,25 @@ int validate_shape(int bh, int S, int hd, float scale, int dtype)
 
 bool tc_supported(int hd, int dtype) { return dtype == XFA_BF16 && (hd == 64 || hd == 128); }
 
-// Resolve the implementation for a call; XFA_OK and *use_tc set on success.
-int choose_impl(int impl, int hd, int dtype, bool *use_tc)
+enum class Family { Simt, TcFused, TcDet };
+
+// The tcgen05 backward variant XFA_IMPL_AUTO resolves to.
+constexpr Family kAutoTc = Family::TcFused;
+
+// Resolve the implementation for a call; XFA_OK and *fam set on success.
+int choose_impl(int impl, int hd, int dtype, Family *fam)
 {
     switch (impl) {
-    case XFA_IMPL_SIMT: *use_tc = false; return XFA_OK;
+    case XFA_IMPL_SIMT: *fam = Family::Simt; return XFA_OK;
     case XFA_IMPL_TCGEN05:
+    case XFA_IMPL_TCGEN05_DET:
         if (!tc_supported(hd, dtype)) return XFA_ERR_UNSUPPORTED;
         if (!device_is_sm103()) return XFA_ERR_DEVICE;
-        *use_tc = true;
+        *fam = impl == XFA_IMPL_TCGEN05 ? Family::TcFused : Family::TcDet;
         return XFA_OK;
-    case XFA_IMPL_AUTO: *use_tc = tc_supported(hd, dtype) && device_is_sm103(); return XFA_OK;
+    case XFA_IMPL_AUTO:
+        *fam = (tc_supported(hd, dtype) && device_is_sm103()) ? kAutoTc : Family::Simt;
+        return XFA_OK;
     default: return XFA_ERR_INVALID_ARG;
     }
 }
@@ -178,12 +186,12 @@ int xfa_fwd_impl(const void *q, const void *k, const void *v, void *out, float *
     if (rc != XFA_OK) return rc;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
         return XFA_ERR_INVALID_ARG;
-    bool use_tc = false;
-    if ((rc = choose_impl(impl, hd, dtype, &use_tc)) != XFA_OK) return rc;
+    Family fam;
+    if ((rc = choose_impl(impl, hd, dtype, &fam)) != XFA_OK) return rc;
     FwdParams p{q, k, v, out, lse, bh, S, hd, scale, dtype, nullptr};
     if ((rc = status_ptr(&p.status)) != XFA_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (use_tc) return launch_tc_fwd(p, st);
+    if (fam != Family::Simt) return launch_tc_fwd(p, st);
     return cuda_code(launch_simt_fwd(p, st));
 }
 
@@ -226,15 +234,43 @@ static int bwd_setup(BwdParams &p, const void *q, const void *k, const void *v, 
 // Any 16-byte aligned non-null placeholder for pointers a stage does not touch.
 static const void *unused_ptr(const void *p) { return p; }
 
+// The three stages of one backward for the resolved family.
+static int stage_prep(BwdParams p, Family fam, cudaStream_t st)
+{
+    if (fam == Family::TcDet) p.dq_acc = nullptr;   // no accumulator to clear
+    return cuda_code(launch_bwd_prep(p, st));
+}
+
+static int stage_main(const BwdParams &p, Family fam, cudaStream_t st)
+{
+    switch (fam) {
+    case Family::Simt: return cuda_code(launch_simt_bwd(p, st));
+    case Family::TcFused: return launch_tc_bwd(p, st, true);
+    case Family::TcDet: {
+        int rc = launch_tc_bwd(p, st, false);
+        return rc == XFA_OK ? launch_tc_dq(p, st) : rc;
+    }
+    }
+    return XFA_ERR_INVALID_ARG;
+}
+
+static int stage_finish(const BwdParams &p, Family fam, cudaStream_t st)
+{
+    if (p.dtype != XFA_BF16 || fam == Family::TcDet) return XFA_OK;
+    return cuda_code(launch_convert_dq(p.dq_acc, p.dq, (size_t)p.bh * p.S * p.hd, p.dtype, st));
+}
+
 int xfa_bwd_prep(const void *out, const void *dout, const float *lse, void *dq, int bh, int S, int hd, int dtype,
-                 void *workspace, size_t workspace_bytes, void *stream)
+                 void *workspace, size_t workspace_bytes, int impl, void *stream)
 {
     BwdParams p;
     const void *u = unused_ptr(out);
     int rc = bwd_setup(p, u, u, u, out, dout, lse, dq, const_cast<void *>(u), const_cast<void *>(u), bh, S, hd,
                        1.0f, dtype, workspace, workspace_bytes);
     if (rc != XFA_OK) return rc;
-    return cuda_code(launch_bwd_prep(p, static_cast<cudaStream_t>(stream)));
+    Family fam;
+    if ((rc = choose_impl(impl, hd, dtype, &fam)) != XFA_OK) return rc;
+    return stage_prep(p, fam, static_cast<cudaStream_t>(stream));
 }
 
 int xfa_bwd_main(const void *q, const void *k, const void *v, const void *dout, void *dq, void *dk, void *dv, int bh,
@@ -245,20 +281,21 @@ int xfa_bwd_main(const void *q, const void *k, const void *v, const void *dout, 
     int rc = bwd_setup(p, q, k, v, dout, dout, reinterpret_cast<const float *>(workspace), dq, dk, dv, bh, S, hd,
                        scale, dtype, workspace, workspace_bytes);
     if (rc != XFA_OK) return rc;
-    bool use_tc = false;
-    if ((rc = choose_impl(impl, hd, dtype, &use_tc)) != XFA_OK) return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return use_tc ? launch_tc_bwd(p, st) : cuda_code(launch_simt_bwd(p, st));
+    Family fam;
+    if ((rc = choose_impl(impl, hd, dtype, &fam)) != XFA_OK) return rc;
+    return stage_main(p, fam, static_cast<cudaStream_t>(stream));
 }
 
-int xfa_bwd_finish(void *dq, int bh, int S, int hd, int dtype, void *workspace, size_t workspace_bytes, void *stream)
+int xfa_bwd_finish(void *dq, int bh, int S, int hd, int dtype, void *workspace, size_t workspace_bytes, int impl,
+                   void *stream)
 {
     BwdParams p;
     int rc = bwd_setup(p, dq, dq, dq, dq, dq, reinterpret_cast<const float *>(workspace), dq, dq, dq, bh, S, hd, 1.0f,
                        dtype, workspace, workspace_bytes);
     if (rc != XFA_OK) return rc;
-    if (dtype != XFA_BF16) return XFA_OK;
-    return cuda_code(launch_convert_dq(p.dq_acc, dq, (size_t)bh * S * hd, dtype, static_cast<cudaStream_t>(stream)));
+    Family fam;
+    if ((rc = choose_impl(impl, hd, dtype, &fam)) != XFA_OK) return rc;
+    return stage_finish(p, fam, static_cast<cudaStream_t>(stream));
 }
 
 int xfa_bwd_impl(const void *q, const void *k, const void *v, const void *out, const void *dout, const float *lse,
@@ -268,14 +305,12 @@ int xfa_bwd_impl(const void *q, const void *k, const void *v, const void *out, c
     BwdParams p;
     int rc = bwd_setup(p, q, k, v, out, dout, lse, dq, dk, dv, bh, S, hd, scale, dtype, workspace, workspace_bytes);
     if (rc != XFA_OK) return rc;
-    bool use_tc = false;
-    if ((rc = choose_impl(impl, hd, dtype, &use_tc)) != XFA_OK) return rc;
+    Family fam;
+    if ((rc = choose_impl(impl, hd, dtype, &fam)) != XFA_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if ((rc = cuda_code(launch_bwd_prep(p, st))) != XFA_OK) return rc;
-    rc = use_tc ? launch_tc_bwd(p, st) : cuda_code(launch_simt_bwd(p, st));
-    if (rc != XFA_OK) return rc;
-    if (dtype == XFA_BF16) rc = cuda_code(launch_convert_dq(p.dq_acc, dq, (size_t)bh * S * hd, dtype, st));
-    return rc;
+    if ((rc = stage_prep(p, fam, st)) != XFA_OK) return rc;
+    if ((rc = stage_main(p, fam, st)) != XFA_OK) return rc;
+    return stage_finish(p, fam, st);
 }
 
 int xfa_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout, const float *lse,

@@ -50,9 +50,13 @@ typedef enum { XFA_F32 = 0, XFA_BF16 = 1 } xfa_dtype;
 
 /* Kernel family selector for the *_impl entry points. */
 typedef enum {
-    XFA_IMPL_AUTO = 0,    /* tcgen05 tensor-core kernels where supported, else SIMT */
-    XFA_IMPL_SIMT = 1,    /* fp32 FFMA tiled kernels (every dtype and hd) */
-    XFA_IMPL_TCGEN05 = 2  /* bf16, hd in {64, 128}: TMA + tcgen05.mma + TMEM kernels */
+    XFA_IMPL_AUTO = 0,        /* the fastest tcgen05 variant where supported, else SIMT */
+    XFA_IMPL_SIMT = 1,        /* fp32 FFMA tiled kernels (every dtype and hd) */
+    XFA_IMPL_TCGEN05 = 2,     /* bf16, hd in {64, 128}: TMA + tcgen05.mma + TMEM kernels; the
+                                 backward sums dQ over key tiles with fp32 reductions, so dQ may
+                                 differ in the last bits from run to run */
+    XFA_IMPL_TCGEN05_DET = 3  /* as XFA_IMPL_TCGEN05, but the backward forms dQ in a separate
+                                 query-tile pass without atomics: bit-reproducible results */
 } xfa_impl;
 
 enum {
@@ -123,18 +127,21 @@ int xfa_bwd_impl(const void *q, const void *k, const void *v, const void *out, c
  * in this order on one stream, with the same arguments and workspace.
  *   prep   : D_i = dO_i . O_i and -L_i * log2(e) into the workspace (padded
  *            rows: D = 0, -L*log2(e) = -inf), and clears the fp32 dQ accumulator (the
- *            workspace for bf16, dq itself for fp32).
- *   main   : the backward kernel (dK, dV written; dQ summed into the accumulator).
- *   finish : dQ accumulator -> dq in the output dtype (nothing to do for fp32).
+ *            workspace for bf16, dq itself for fp32) when the implementation uses one.
+ *   main   : the backward kernels: dK, dV written; dQ summed into the accumulator,
+ *            or (XFA_IMPL_TCGEN05_DET) written directly by the query-tile dQ pass.
+ *   finish : dQ accumulator -> dq in the output dtype (nothing to do for fp32 or
+ *            for XFA_IMPL_TCGEN05_DET).
+ * `impl` must be the same for the three stages of one backward.
  * Same argument rules and error codes as xfa_bwd.
  */
 int xfa_bwd_prep(const void *out, const void *dout, const float *lse, void *dq, int bh, int S, int hd, int dtype,
-                 void *workspace, size_t workspace_bytes, void *stream);
+                 void *workspace, size_t workspace_bytes, int impl, void *stream);
 int xfa_bwd_main(const void *q, const void *k, const void *v, const void *dout, void *dq, void *dk, void *dv,
                  int bh, int S, int hd, float scale, int dtype, void *workspace, size_t workspace_bytes, int impl,
                  void *stream);
 int xfa_bwd_finish(void *dq, int bh, int S, int hd, int dtype, void *workspace, size_t workspace_bytes,
-                   void *stream);
+                   int impl, void *stream);
 
 /*
  * Size in bytes of the fixed device scratch array used by xfa_bwd_noalloc.

@@ -49,11 +49,12 @@ def _identities(got, x, dtype):
     assert np.all(np.abs(tq - tk) <= tol * mag), "tr(Q^T dQ) != tr(K^T dK)"
 
 
+@pytest.mark.parametrize("impl", [0, 3], ids=["auto", "deterministic"])
 @pytest.mark.parametrize("wid,heads", [(4, (0, 37, 63)), (5, (0, 31))])
-def test_workload_full_size_sampled(wid, heads):
+def test_workload_full_size_sampled(wid, heads, impl):
     w = inputs.WORKLOADS[wid]
     x = inputs.workload_inputs(w)
-    got = run_gpu(x, w.dtype, w.scale)
+    got = run_gpu(x, w.dtype, w.scale, impl=impl)
     for n in ("out", "lse", "dq", "dk", "dv"):
         assert np.all(np.isfinite(got[n])), n
     ref = oracle_result(("w", wid), x, w.scale, heads=list(heads))
@@ -65,8 +66,9 @@ RAGGED = [1, 5, 64, 100, 128, 129, 255, 256, 257, 300, 511, 777]
 
 
 @pytest.mark.parametrize("S", RAGGED)
-@pytest.mark.parametrize("dtype,hd,impl", [("bf16", 128, 2), ("bf16", 64, 2), ("bf16", 32, 1), ("f32", 32, 1),
-                                           ("f32", 64, 1), ("f32", 128, 1), ("bf16", 128, 1)])
+@pytest.mark.parametrize("dtype,hd,impl", [("bf16", 128, 2), ("bf16", 64, 2), ("bf16", 128, 3), ("bf16", 64, 3),
+                                           ("bf16", 32, 1), ("f32", 32, 1), ("f32", 64, 1), ("f32", 128, 1),
+                                           ("bf16", 128, 1)])
 def test_ragged_and_small(S, dtype, hd, impl):
     bh = 3
     scale = 1.0 / math.sqrt(hd)
@@ -82,7 +84,7 @@ def test_tcgen05_and_simt_agree_with_oracle(hd):
     scale = 1.0 / math.sqrt(hd)
     x = inputs.draw((bh, S, hd), "bf16", seed=77 + hd, stds=(2.0, 2.0, 1.0, 1.0))
     ref = oracle_result(("both", hd), x, scale)
-    for impl in (1, 2):
+    for impl in (1, 2, 3):
         compare(run_gpu(x, "bf16", scale, impl=impl), ref, "bf16")
 
 
@@ -110,7 +112,7 @@ def test_outputs_do_not_write_outside_their_buffers():
         buf = torch.full((numel + 2 * guard,), -7.0, device="cuda", dtype=dtype)
         return buf, buf[guard:guard + numel]
 
-    for impl in (1, 2):
+    for impl in (1, 2, 3):
         bo, out = guarded(n, torch.bfloat16)
         bl, lse = guarded(bh * S, torch.float32)
         binding.fwd(q, k, v, scale, impl, out=out.view(bh, S, hd), lse=lse.view(bh, S))
@@ -135,6 +137,39 @@ def test_backward_is_repeatable_with_reused_workspace():
     for s, t in zip(a, b):
         # dQ is summed with fp32 atomics in a data-dependent order: equal up to rounding
         assert torch.allclose(s.float(), t.float(), rtol=0, atol=1e-2 * float(s.float().abs().max()))
+
+
+@pytest.mark.parametrize("hd,S", [(128, 1000), (64, 777)])
+def test_deterministic_backward_is_bit_reproducible(hd, S):
+    """XFA_IMPL_TCGEN05_DET forms dQ without atomics: two runs give identical bits."""
+    from bwd_xfa_fwd_gb300 import binding
+    bh = 6
+    x = inputs.draw((bh, S, hd), "bf16", seed=31 + hd)
+    q, k, v, do = (to_device(x[n], "bf16") for n in ("q", "k", "v", "dout"))
+    out, lse = binding.fwd(q, k, v, impl=binding.IMPL_TCGEN05_DET)
+    a = [t.clone() for t in binding.bwd(q, k, v, out, do, lse, impl=binding.IMPL_TCGEN05_DET)]
+    for _ in range(2):
+        b = binding.bwd(q, k, v, out, do, lse, impl=binding.IMPL_TCGEN05_DET)
+        for s_, t_ in zip(a, b):
+            assert torch.equal(s_, t_)
+
+
+def test_bwd_stages_match_bwd_for_every_impl():
+    """prep/main/finish called one by one give what xfa_bwd gives, for each kernel family."""
+    from bwd_xfa_fwd_gb300 import binding
+    bh, S, hd = 3, 300, 128
+    scale = 1.0 / math.sqrt(hd)
+    x = inputs.draw((bh, S, hd), "bf16", seed=41)
+    q, k, v, do = (to_device(x[n], "bf16") for n in ("q", "k", "v", "dout"))
+    for impl in (1, 2, 3):
+        out, lse = binding.fwd(q, k, v, scale, impl)
+        whole = binding.bwd(q, k, v, out, do, lse, scale, impl)
+        ws = torch.empty(binding.workspace_bytes(bh, S, hd, q.dtype), device="cuda", dtype=torch.uint8)
+        grads = tuple(torch.empty_like(q) for _ in range(3))
+        staged = binding.bwd_stages(q, k, v, out, do, lse, scale, ws, grads, impl=impl)
+        torch.cuda.synchronize()
+        for a_, b_ in zip(whole, staged):
+            assert torch.allclose(a_.float(), b_.float(), rtol=0, atol=1e-2 * float(a_.float().abs().max()))
 
 
 def test_unsupported_combinations_are_rejected():
