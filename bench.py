@@ -77,6 +77,18 @@ def recorded_traffic(name, workload):
     return e["dram_bytes_per_launch"]
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest `value` over all ranks of the default process group (the
+    value itself when no group is initialised)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
         os.environ.get("LOCAL_RANK", "0"))
@@ -235,11 +247,7 @@ def run_ours(args, w):
         torch.distributed.barrier()
     if binding.status() != binding.XFA_OK:
         raise RuntimeError("kernel status not ok after the timed region")
-    total_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), device="cuda")
     per = {s: float(np.mean([a.elapsed_time(b) for a, b in ev[s]])) for s in stages}
     ms_step = total_ms / K
     f_fwd, f_bwd = w.fwd_flops(), w.bwd_flops()
