@@ -204,3 +204,33 @@ def test_tape_node_fanout_on_gpu():
     got = {"out": to_f64(y.value), "dq": to_f64(xv.grad)}
     want = {"out": ref["out"], "dq": ref["dq"] + ref["dk"] + ref["dv"]}
     compare(got, want, "bf16", names=("out", "dq"))
+
+
+def test_runs_on_the_callers_stream():
+    """Every call is enqueued on the current torch stream (a side stream here); results
+    match the oracle and nothing runs on the default stream."""
+    from bwd_xfa_fwd_gb300 import binding
+    bh, S, hd = 2, 640, 128
+    scale = 1.0 / math.sqrt(hd)
+    x = inputs.draw((bh, S, hd), "bf16", seed=55)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        q, k, v, do = (to_device(x[n], "bf16") for n in ("q", "k", "v", "dout"))
+        out, lse = binding.fwd(q, k, v, scale)
+        dq, dk, dv = binding.bwd(q, k, v, out, do, lse, scale)
+    side.synchronize()
+    got = {n: to_f64(t) for n, t in zip(("out", "lse", "dq", "dk", "dv"), (out, lse, dq, dk, dv))}
+    compare(got, oracle_result(("side",), x, scale), "bf16")
+
+
+def test_tape_node_with_deterministic_backward():
+    from bwd_xfa_fwd_gb300 import binding
+    from bwd_xfa_fwd_gb300.tape import Var, flash_attention
+    bh, S, hd = 2, 300, 64
+    scale = 1.0 / math.sqrt(hd)
+    x = inputs.draw((bh, S, hd), "bf16", seed=61)
+    qv, kv, vv = (Var(to_device(x[n], "bf16")) for n in ("q", "k", "v"))
+    y = flash_attention(qv, kv, vv, scale, impl=binding.IMPL_TCGEN05_DET)
+    y.backward(seed=to_device(x["dout"], "bf16"))
+    got = {"out": to_f64(y.value), "dq": to_f64(qv.grad), "dk": to_f64(kv.grad), "dv": to_f64(vv.grad)}
+    compare(got, oracle_result(("tape-det",), x, scale), "bf16", names=("out", "dq", "dk", "dv"))
