@@ -292,15 +292,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 128; ++c)
                     if (c > r) sr[c] = 0xff800000u;   // -inf
             }
-            // row max: 4 independent chains of 3-input maxima
+            // row max: 4 independent chains of 3-input maxima over columns 0..127
+            // (chain e starts at column e, then takes two columns per step from 4 + 8k + 2e;
+            // the last four columns 124..127 are folded in singly)
             float mx4[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) mx4[e] = __uint_as_float(sr[e]);
 #pragma unroll
-            for (int c = 4; c < 128; c += 8)
+            for (int c = 4; c + 8 <= 124; c += 8)
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     mx4[e] = fmax3(mx4[e], __uint_as_float(sr[c + 2 * e]), __uint_as_float(sr[c + 2 * e + 1]));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mx4[e] = fmaxf(mx4[e], __uint_as_float(sr[124 + e]));
             const float mx = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
             const float m_new = fmaxf(m, mx * scale_log2);   // scale > 0: max commutes with the scaling
             const bool need = m_new > m + kRescaleThreshold;

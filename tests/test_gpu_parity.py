@@ -234,3 +234,27 @@ def test_tape_node_with_deterministic_backward():
     y.backward(seed=to_device(x["dout"], "bf16"))
     got = {"out": to_f64(y.value), "dq": to_f64(qv.grad), "dk": to_f64(kv.grad), "dv": to_f64(vv.grad)}
     compare(got, oracle_result(("tape-det",), x, scale), "bf16", names=("out", "dq", "dk", "dv"))
+
+
+def _fuzz_cases(n=24, seed=2024):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        dtype = "bf16" if i % 4 else "f32"
+        hd = int(rng.choice([64, 128])) if dtype == "bf16" else int(rng.choice([32, 64, 128]))
+        impl = int(rng.choice([0, 2, 3])) if dtype == "bf16" else 1
+        S = int(rng.integers(1, 1400))
+        bh = int(rng.integers(1, 5))
+        scale = float(rng.uniform(0.02, 0.3))
+        std = float(rng.choice([0.5, 1.0, 2.0, 3.0]))
+        cases.append((i, dtype, hd, impl, S, bh, scale, std))
+    return cases
+
+
+@pytest.mark.parametrize("case", _fuzz_cases(), ids=lambda c: f"{c[0]}-{c[1]}-hd{c[2]}-impl{c[3]}-S{c[4]}-bh{c[5]}")
+def test_random_shapes_against_oracle(case):
+    """Seeded random shapes, scales, input spreads and kernel families."""
+    i, dtype, hd, impl, S, bh, scale, std = case
+    x = inputs.draw((bh, S, hd), dtype, seed=7000 + i, stds=(std, std, 1.0, 1.0))
+    got = run_gpu(x, dtype, scale, impl=impl)
+    compare(got, oracle_result(("fuzz", i), x, scale), dtype)
