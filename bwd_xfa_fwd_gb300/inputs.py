@@ -78,6 +78,13 @@ class Tensors:
     exact: np.ndarray
 
 
+def _stored(x32: np.ndarray, dtype: str) -> Tensors:
+    if dtype == "f32":
+        return Tensors(x32, x32.astype(np.float64))
+    bits = f32_to_bf16_bits(x32)
+    return Tensors(bits, bf16_bits_to_f64(bits))
+
+
 def draw(shape, dtype: str, seed: int, stds=(1.0, 1.0, 1.0, 1.0), names=("q", "k", "v", "dout")):
     """Draw the named tensors in order from one generator seeded with ``seed``."""
     if dtype not in ("f32", "bf16"):
@@ -86,13 +93,50 @@ def draw(shape, dtype: str, seed: int, stds=(1.0, 1.0, 1.0, 1.0), names=("q", "k
     out = {}
     for name, std in zip(names, stds):
         x32 = (rng.standard_normal(shape) * std).astype(np.float32)
-        if dtype == "f32":
-            out[name] = Tensors(x32, x32.astype(np.float64))
-        else:
-            bits = f32_to_bf16_bits(x32)
-            del x32
-            out[name] = Tensors(bits, bf16_bits_to_f64(bits))
+        out[name] = _stored(x32, dtype)
+        del x32
     return out
+
+
+PATTERNS = ("rising", "falling", "flat")
+
+
+def patterned(shape, dtype: str, pattern: str, seed: int, magnitude: float = 16.0, k_noise: float = 2.0):
+    """Structured Q and K (V and dO standard normal) for the score shapes that steer the
+    online softmax.  Q and K rows have norm ``magnitude`` in the plane of coordinates 0
+    and 1, at angle theta_j = pi * j / S for position j:
+      "rising":  q_i at theta_i and k_j at theta_j, so s_ij ~ cos(pi (i - j) / S): along a
+                 row the scores climb towards the diagonal and the running row maximum
+                 keeps moving;
+      "falling": q_i fixed at angle 0 and k_j at theta_j, so the scores fall along the row
+                 and its maximum is the first key;
+      "flat":    Q = 0, all scores equal.
+    The norms stay constant along the sequence.  The other coordinates of K carry
+    independent N(0, k_noise^2) values, as keys do, and those of Q N(0, 0.1^2) noise, so
+    the scores follow the pattern while the keys that share a row's softmax window are
+    not nearly parallel (with parallel keys dQ = sum_j dS_ij (K_j - K_i) is a near
+    cancellation that any bf16 rounding of dS exposes)."""
+    if pattern not in PATTERNS:
+        raise ValueError(f"unknown pattern {pattern!r}")
+    bh, S, hd = shape
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal(shape) * 0.1
+    k = rng.standard_normal(shape) * k_noise
+    v = rng.standard_normal(shape)
+    do = rng.standard_normal(shape)
+    theta = np.pi * np.arange(S, dtype=np.float64) / S
+    if pattern == "flat":
+        q[:] = 0.0
+    else:
+        k[..., 0] = magnitude * np.cos(theta)
+        k[..., 1] = magnitude * np.sin(theta)
+        if pattern == "rising":
+            q[..., 0] = magnitude * np.cos(theta)
+            q[..., 1] = magnitude * np.sin(theta)
+        else:
+            q[..., 0] = magnitude
+            q[..., 1] = 0.0
+    return {n: _stored(a.astype(np.float32), dtype) for n, a in (("q", q), ("k", k), ("v", v), ("dout", do))}
 
 
 def workload_inputs(w: Workload, bh: int | None = None, S: int | None = None):
