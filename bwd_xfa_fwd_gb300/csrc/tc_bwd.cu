@@ -96,6 +96,44 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, Bars *
     return ok;
 }
 
+// Epilogue of one 128-row accumulator (dK or dV): thread r (TMEM lane r) converts its row of
+// hd fp32 columns to bf16 and writes it into `stage`, laid out as the 128-byte-swizzled TMA box
+// ([hd / 64][128 rows][128 B], 16-byte chunk c of row r at chunk c ^ (r & 7)); once the 128
+// threads of the group (named barrier `bar_id`) are through, `issuer` stores the tile with TMA
+// (rows past the tensor's extent are not written) and waits until the stores have read the
+// staging tile; their writes complete before the grid does.
+template <int HD>
+__device__ __forceinline__ void store_rows_tma(uint32_t t_row, uint8_t *stage, int r, const CUtensorMap *map, int y,
+                                               int z, uint32_t bar_id, bool issuer)
+{
+#pragma unroll 1
+    for (int c = 0; c < HD; c += 32) {
+        uint32_t o[32];
+        tmem_ld32(t_row + c, o);
+        tmem_wait_ld();
+        reg_fence32(o);
+        uint8_t *row = stage + (c / 64) * (128 * 128) + r * 128;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]), __uint_as_float(o[8 * v + 1]));
+            w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]), __uint_as_float(o[8 * v + 3]));
+            w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]), __uint_as_float(o[8 * v + 5]));
+            w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]), __uint_as_float(o[8 * v + 7]));
+            const int chunk = (c % 64) / 8 + v;
+            *reinterpret_cast<uint4 *>(row + ((chunk ^ (r & 7)) << 4)) = w;
+        }
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(bar_id, 128);
+    if (issuer) {
+#pragma unroll
+        for (int s = 0; s < HD / 64; ++s) tma_store_3d(map, stage + s * 128 * 128, s * 64, y, z);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+    }
+}
+
 // C[M=128, N=64] = A[128 rows x hd] * B[64 rows x hd]^T, both K-major (hd contiguous);
 // descriptors of the tile bases, advanced per 16-wide K step.
 template <int HD>
@@ -126,6 +164,7 @@ template <int HD, bool FUSED_DQ>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                   const float *__restrict__ Lg, const float *__restrict__ Dg, float *__restrict__ dq_acc,
                   __nv_bfloat16 *__restrict__ dK, __nv_bfloat16 *__restrict__ dV, int bh, int S, int S_pad,
                   float scale, float scale_log2, int *status)
@@ -421,28 +460,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->ds_full[b]);
         }
-        // epilogue: dV rows
-        if (ok && warp_wait(&bars->done, 0, bars, status)) {
+        // epilogue: dV rows, staged in the query-tile ring (free once every MMA has completed);
+        // the four warps decide together, since the staging ends in a barrier of all 128 threads
+        if (named_bar_and(2, 128, ok && warp_wait(&bars->done, 0, bars, status))) {
             tc_fence_after_sync();
-            __nv_bfloat16 *dst = dV + ((size_t)head * S + key) * HD;
-#pragma unroll 1
-            for (int c = 0; c < HD; c += 32) {
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_off + C::COL_DV + c, o);
-                tmem_wait_ld();
-                reg_fence32(o);
-                if (key < S) {
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]), __uint_as_float(o[8 * v + 1]));
-                        w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]), __uint_as_float(o[8 * v + 3]));
-                        w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]), __uint_as_float(o[8 * v + 5]));
-                        w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]), __uint_as_float(o[8 * v + 7]));
-                        reinterpret_cast<uint4 *>(dst + c)[v] = w;
-                    }
-                }
-            }
+            store_rows_tma<HD>(tmem + lane_off + C::COL_DV, smem + C::OFF_Q, r, &tm_dv, j0, head, 2, threadIdx.x == 0);
         }
     } else if (warp < 8) {
         // dQ readout: thread = hd index d (TMEM lane of dQ^T)
@@ -452,7 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         if (FUSED_DQ && d < HD) {
             for (int it = 0; it < n; ++it) {
-                if (!(ok = warp_wait(&bars->dq_full, it & 1, bars, status))) break;
+                // the readout warps stay in step: all leave the loop together if one gives up
+                if (!(ok = named_bar_and(1, HD, warp_wait(&bars->dq_full, it & 1, bars, status)))) break;
                 tc_fence_after_sync();
                 uint32_t g[64];
                 tmem_ld32(tmem + lane_off + C::COL_DQ, g);
@@ -477,31 +500,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bulk_commit_group();
                 }
             }
-            if (d == 0) bulk_wait_group0();
+            if (d == 0) bulk_wait_group_read0();   // the staging tile is read; the adds complete before the grid does
         }
-        // epilogue: dK rows (same TMEM lanes as warps 0-3: thread = key)
-        const int key = j0 + wq * 32 + lane;
-        if (ok && warp_wait(&bars->done, 0, bars, status)) {
+        // epilogue: dK rows (same TMEM lanes as warps 0-3: thread = key), staged in the dO ring;
+        // decided together by the four warps, as for dV
+        if (named_bar_and(3, 128, ok && warp_wait(&bars->done, 0, bars, status))) {
             tc_fence_after_sync();
-            __nv_bfloat16 *dst = dK + ((size_t)head * S + key) * HD;
-#pragma unroll 1
-            for (int c = 0; c < HD; c += 32) {
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_off + C::COL_DK + c, o);
-                tmem_wait_ld();
-                reg_fence32(o);
-                if (key < S) {
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]), __uint_as_float(o[8 * v + 1]));
-                        w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]), __uint_as_float(o[8 * v + 3]));
-                        w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]), __uint_as_float(o[8 * v + 5]));
-                        w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]), __uint_as_float(o[8 * v + 7]));
-                        reinterpret_cast<uint4 *>(dst + c)[v] = w;
-                    }
-                }
-            }
+            store_rows_tma<HD>(tmem + lane_off + C::COL_DK, smem + C::OFF_DO, wq * 32 + lane, &tm_dk, j0, head, 3,
+                               wq == 0 && lane == 0);
         }
     }
 
@@ -516,19 +522,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int HD, bool FUSED_DQ>
 int run(const BwdParams &p, cudaStream_t st)
 {
-    alignas(64) CUtensorMap tk, tv, tq, tdo;
+    alignas(64) CUtensorMap tk, tv, tq, tdo, tdk, tdv;
     int rc = encode_tmap_bf16_3d(&tk, p.k, HD, p.S, p.bh, BN);
     if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tv, p.v, HD, p.S, p.bh, BN);
     if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tq, p.q, HD, p.S, p.bh, BM);
     if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tdo, p.dout, HD, p.S, p.bh, BM);
+    if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tdk, p.dk, HD, p.S, p.bh, BN);
+    if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tdv, p.dv, HD, p.S, p.bh, BN);
     if (rc != XFA_OK) return rc;
     static_assert(Cfg<HD>::SMEM <= 227 * 1024, "shared memory per CTA");
+    static_assert(Cfg<HD>::NSQ * Cfg<HD>::Q_BYTES >= Cfg<HD>::KV_BYTES, "dK / dV staging fits a ring");
     auto kern = tc_bwd_kernel<HD, FUSED_DQ>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<HD>::SMEM);
     if (e != cudaSuccess) return XFA_ERR_CUDA_BASE + (int)e;
     const int nkt = (p.S + BN - 1) / BN;
     const unsigned grid = (unsigned)(nkt * p.bh);
-    kern<<<grid, kThreads, Cfg<HD>::SMEM, st>>>(tk, tv, tq, tdo, p.Lg, p.D, p.dq_acc, (__nv_bfloat16 *)p.dk,
+    kern<<<grid, kThreads, Cfg<HD>::SMEM, st>>>(tk, tv, tq, tdo, tdk, tdv, p.Lg, p.D, p.dq_acc, (__nv_bfloat16 *)p.dk,
                                                  (__nv_bfloat16 *)p.dv, p.bh, p.S, p.S_pad, p.scale,
                                                  p.scale * 1.4426950408889634f, p.status);
     e = cudaGetLastError();
