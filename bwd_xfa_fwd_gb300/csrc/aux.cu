@@ -128,15 +128,25 @@ cudaError_t rowdot_any(const void *O, const void *dO, const float *lse, float *D
     }
 }
 
+// fp32 -> bf16, four independent float4 per thread and step (loads issued first).
 __global__ void __launch_bounds__(256) convert_bf16_kernel(const float4 *__restrict__ src, uint2 *__restrict__ dst,
                                                            size_t n4)
 {
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
-        const float4 v = __ldg(src + i);
-        uint2 o;
-        o.x = pack_bf16x2(v.x, v.y);
-        o.y = pack_bf16x2(v.z, v.w);
-        dst[i] = o;
+    constexpr int U = 4;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n4; i0 += U * stride) {
+        float4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (i0 + u * stride < n4) v[u] = __ldg(src + i0 + u * stride);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (i0 + u * stride < n4) {
+                uint2 o;
+                o.x = pack_bf16x2(v[u].x, v[u].y);
+                o.y = pack_bf16x2(v[u].z, v[u].w);
+                dst[i0 + u * stride] = o;
+            }
     }
 }
 
