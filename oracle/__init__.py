@@ -15,7 +15,11 @@ by ``tests/test_oracle.py``): a hand-worked 2x2 example, the row-sum and
 softmax-backward identities of "xtrain docs/13-flash-attention.md"
 (sections "什么是 flash-attention" and design decision ③), central finite
 differences in fp64, special cases with closed forms (S=1, Q=0, hd=1) and the
-unmasked case against a dense numpy softmax.
+unmasked case against a dense numpy softmax.  The optional dropout on the
+attention probabilities ("xtrain docs/17-dropout.md", section "Key Design
+Decisions") is pinned by ``tests/test_oracle_dropout.py``: known outputs of the
+SplitMix64 generator, the keep rate, p = 0 against the plain path, finite
+differences with the mask fixed, the D identity and the expectation over seeds.
 """
 from __future__ import annotations
 
@@ -71,6 +75,14 @@ class Oracle:
         lib.xfa_oracle_head.argtypes = [dp, dp, dp, dp, ctypes.c_long, ctypes.c_long, ctypes.c_double,
                                         ctypes.c_int, dp, dp, dp, dp, dp, dp, dp, dp]
         lib.xfa_oracle_head.restype = ctypes.c_int
+        lib.xfa_oracle_head_dropout.argtypes = [dp, dp, dp, dp, ctypes.c_long, ctypes.c_long, ctypes.c_double,
+                                                ctypes.c_int, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint64,
+                                                dp, dp, dp, dp, dp, dp, dp, dp]
+        lib.xfa_oracle_head_dropout.restype = ctypes.c_int
+        lib.xfa_oracle_splitmix64.argtypes = [ctypes.c_uint64]
+        lib.xfa_oracle_splitmix64.restype = ctypes.c_uint64
+        lib.xfa_oracle_keep.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_float]
+        lib.xfa_oracle_keep.restype = ctypes.c_int
         lib.xfa_oracle_threads.argtypes = []
         lib.xfa_oracle_threads.restype = ctypes.c_int
         self.lib = lib
@@ -78,7 +90,13 @@ class Oracle:
     def threads(self) -> int:
         return int(self.lib.xfa_oracle_threads())
 
-    def head(self, q, k, v, dout=None, scale=1.0, causal=True, diagnostics=False):
+    def splitmix64(self, x: int) -> int:
+        return int(self.lib.xfa_oracle_splitmix64(x & (2 ** 64 - 1)))
+
+    def keep(self, seed: int, index: int, p: float) -> bool:
+        return bool(self.lib.xfa_oracle_keep(seed & (2 ** 64 - 1), index & (2 ** 64 - 1), p))
+
+    def head(self, q, k, v, dout=None, scale=1.0, causal=True, diagnostics=False, dropout=None):
         """See :func:`attention_head`."""
         q, k, v = _f64(q), _f64(k), _f64(v)
         S, hd = q.shape
@@ -96,10 +114,16 @@ class Oracle:
             if dout is not None:
                 res["pdp_rowsum"] = np.empty(S)
                 res["ds_rowsum"] = np.empty(S)
-        rc = self.lib.xfa_oracle_head(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), S, hd, float(scale),
-                                      int(bool(causal)), _ptr(res["out"]), _ptr(res["lse"]), _ptr(res.get("dq")),
-                                      _ptr(res.get("dk")), _ptr(res.get("dv")), _ptr(res.get("p_rowsum")),
-                                      _ptr(res.get("pdp_rowsum")), _ptr(res.get("ds_rowsum")))
+        outs = (_ptr(res["out"]), _ptr(res["lse"]), _ptr(res.get("dq")), _ptr(res.get("dk")), _ptr(res.get("dv")),
+                _ptr(res.get("p_rowsum")), _ptr(res.get("pdp_rowsum")), _ptr(res.get("ds_rowsum")))
+        if dropout is None:
+            rc = self.lib.xfa_oracle_head(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), S, hd, float(scale),
+                                          int(bool(causal)), *outs)
+        else:
+            p, seed, index_base = dropout
+            rc = self.lib.xfa_oracle_head_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), S, hd, float(scale),
+                                                  int(bool(causal)), float(p), seed & (2 ** 64 - 1),
+                                                  index_base & (2 ** 64 - 1), *outs)
         if rc != 0:
             raise RuntimeError(f"oracle failed with code {rc}")
         return res
@@ -127,18 +151,32 @@ def _f64(a):
     return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
 
 
-def attention_head(q, k, v, dout=None, scale=1.0, causal=True, diagnostics=False):
+def attention_head(q, k, v, dout=None, scale=1.0, causal=True, diagnostics=False, dropout=None):
     """One head, ``q,k,v,dout`` of shape [S, hd].  Returns a dict of fp64 arrays:
     ``out`` [S,hd], ``lse`` [S] (natural log) and, with ``dout``, ``dq, dk, dv``.
     With ``diagnostics`` also ``p_rowsum`` (sum_j P_ij), ``pdp_rowsum``
-    (sum_j P_ij dP_ij) and ``ds_rowsum`` (sum_j dS_ij), one per query row."""
-    return default().head(q, k, v, dout, scale, causal, diagnostics)
+    (sum_j P_ij dP_ij) and ``ds_rowsum`` (sum_j dS_ij), one per query row.
+    ``dropout = (p, seed, index_base)`` applies dropout of rate p to the attention
+    probabilities, element (i, j) drawn with flat index index_base + i*S + j."""
+    return default().head(q, k, v, dout, scale, causal, diagnostics, dropout)
 
 
-def attention(q, k, v, dout=None, scale=1.0, causal=True, heads=None):
+def splitmix64(x: int) -> int:
+    """One step of the SplitMix64 generator from state ``x`` (the dropout page's bit mix)."""
+    return default().splitmix64(x)
+
+
+def keep(seed: int, index: int, p: float) -> bool:
+    """The dropout page's keep decision for element ``index`` under ``seed`` and rate ``p``."""
+    return default().keep(seed, index, p)
+
+
+def attention(q, k, v, dout=None, scale=1.0, causal=True, heads=None, dropout=None):
     """Batched over the leading ``bh`` axis of [bh, S, hd] arrays.  ``heads``
     restricts the computation to a list of head indices (the others are left
-    as NaN), which is how the full-size configurations are sampled."""
+    as NaN), which is how the full-size configurations are sampled.
+    ``dropout = (p, seed)``: dropout on the [bh, S, S] attention probabilities
+    (head b's elements have flat indices b*S*S + i*S + j)."""
     q = np.asarray(q)
     bh, S, hd = q.shape
     heads = list(range(bh)) if heads is None else list(heads)
@@ -147,7 +185,8 @@ def attention(q, k, v, dout=None, scale=1.0, causal=True, heads=None):
         for n in ("dq", "dk", "dv"):
             res[n] = np.full((bh, S, hd), np.nan)
     for b in heads:
-        r = attention_head(q[b], k[b], v[b], None if dout is None else dout[b], scale, causal)
+        dd = None if dropout is None else (dropout[0], dropout[1], b * S * S)
+        r = attention_head(q[b], k[b], v[b], None if dout is None else dout[b], scale, causal, dropout=dd)
         for n, a in r.items():
             res[n][b] = a
     return res

@@ -33,8 +33,22 @@
  * The loops run over every (i, j), masked ones included: exp(-inf) = 0 makes
  * their contribution exactly zero, which keeps the code a literal transcription
  * of the definition.  OpenMP only splits each stage over its output rows.
+ *
+ * Optional dropout on the attention probabilities: the dropout operator of
+ *   "xtrain docs/17-dropout.md" ("Phase T18: Dropout"), section "Key Design
+ *   Decisions" (counter-based RNG, inverted scaling, backward with the same mask)
+ * inserted between the softmax and the product with V:
+ *   Pd = P o C,  C_ij = keep(seed, idx_ij) / (1 - p)     O  = Pd V
+ *   dV = Pd^T dO,  dPd = dO V^T,  dP = dPd o C (the dropout node's backward)
+ * and then the same softmax and scale backward as above.  idx_ij is the flat
+ * index of element (b, i, j) of the [bh, S, S] probability tensor.  The keep
+ * decision follows the page: key = seed XOR (idx * 0x9E3779B97F4A7C15),
+ * h = splitmix64(key), u = (h >> 40) / 2^24 in fp32, keep = (u >= p).  Here
+ * splitmix64(x) is the first output of the SplitMix64 generator started from
+ * state x: the state advances by the golden-ratio increment and is then mixed.
  */
 #include <math.h>
+#include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -79,6 +93,24 @@ static void row_softmax(double *s, long S, double *lse)
     }
 }
 
+/* SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+ * generators", OOPSLA 2014): one step from state x. */
+uint64_t xfa_oracle_splitmix64(uint64_t x)
+{
+    uint64_t z = x + 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+/* The dropout page's Bernoulli draw for element `index`: 1 = keep, 0 = drop. */
+int xfa_oracle_keep(uint64_t seed, uint64_t index, float p)
+{
+    const uint64_t h = xfa_oracle_splitmix64(seed ^ (index * 0x9E3779B97F4A7C15ull));
+    const float u = (float)(h >> 40) / 16777216.0f;
+    return u >= p;
+}
+
 /* c[i][e] = sum_j a[i][j] b[j][e], a [n][n], b [n][w] */
 static void matmul_nn(const double *a, const double *b, long n, long w, double *c)
 {
@@ -121,28 +153,35 @@ static void matmul_nt(const double *a, const double *b, long n, long w, double *
 /*
  * One head.  q, k, v, dout: [S][hd] fp64 row-major.  Outputs (caller-owned):
  *   out [S][hd], lse [S]; when dout != NULL also dq, dk, dv [S][hd].
+ * C: NULL, or the [S][S] dropout factors applied to P before the product with V.
  * Optional diagnostics (NULL to skip), one value per query row i:
  *   p_rowsum[i]   = sum_j P_ij
  *   pdp_rowsum[i] = sum_j P_ij dP_ij   (the softmax-backward row term)
  *   ds_rowsum[i]  = sum_j dS_ij
- * causal != 0 applies the mask j > i -> -inf; causal == 0 is plain dense
- * softmax attention (used only by a test that compares against a library
- * routine).  Returns 0, or nonzero on a bad argument / allocation failure.
  */
-int xfa_oracle_head(const double *q, const double *k, const double *v, const double *dout,
-                    long S, long hd, double scale, int causal,
-                    double *out, double *lse, double *dq, double *dk, double *dv,
-                    double *p_rowsum, double *pdp_rowsum, double *ds_rowsum)
+static int head_impl(const double *q, const double *k, const double *v, const double *dout, long S, long hd,
+                     double scale, int causal, const double *C, double *out, double *lse, double *dq, double *dk,
+                     double *dv, double *p_rowsum, double *pdp_rowsum, double *ds_rowsum)
 {
     if (!q || !k || !v || !out || !lse || S < 1 || hd < 1) return ORACLE_BAD_ARG;
     if (dout && (!dq || !dk || !dv)) return ORACLE_BAD_ARG;
 
     double *P = (double *)malloc(sizeof(double) * (size_t)S * (size_t)S);
     if (!P) return ORACLE_NO_MEMORY;
+    double *Pd = NULL;   /* P o C when dropout is on */
+    if (C) {
+        Pd = (double *)malloc(sizeof(double) * (size_t)S * (size_t)S);
+        if (!Pd) {
+            free(P);
+            return ORACLE_NO_MEMORY;
+        }
+    }
 
     scores(q, k, S, hd, scale, causal, P);  /* P holds s */
     row_softmax(P, S, lse);                 /* P holds softmax(s) */
-    matmul_nn(P, v, S, hd, out);            /* O = P V */
+    if (C)                                  /* the dropout node's forward */
+        for (long e = 0; e < S * S; ++e) Pd[e] = P[e] * C[e];
+    matmul_nn(C ? Pd : P, v, S, hd, out);   /* O = P V (or Pd V) */
 
     if (p_rowsum) {
         for (long i = 0; i < S; ++i) {
@@ -156,10 +195,13 @@ int xfa_oracle_head(const double *q, const double *k, const double *v, const dou
         double *dP = (double *)malloc(sizeof(double) * (size_t)S * (size_t)S);
         if (!dP) {
             free(P);
+            free(Pd);
             return ORACLE_NO_MEMORY;
         }
-        matmul_tn(P, dout, S, hd, dv);   /* dV = P^T dO */
-        matmul_nt(dout, v, S, hd, dP);   /* dP = dO V^T */
+        matmul_tn(C ? Pd : P, dout, S, hd, dv);   /* dV = P^T dO (or Pd^T dO) */
+        matmul_nt(dout, v, S, hd, dP);            /* dP = dO V^T */
+        if (C)                                    /* the dropout node's backward */
+            for (long e = 0; e < S * S; ++e) dP[e] *= C[e];
 
         /* softmax backward, then the scale node's backward, in place in dP */
 #pragma omp parallel for schedule(static) if (S >= 64)
@@ -181,7 +223,45 @@ int xfa_oracle_head(const double *q, const double *k, const double *v, const dou
         free(dP);
     }
     free(P);
+    free(Pd);
     return ORACLE_OK;
+}
+
+/*
+ * causal != 0 applies the mask j > i -> -inf; causal == 0 is plain dense
+ * softmax attention (used only by a test that compares against a library
+ * routine).  Returns 0, or nonzero on a bad argument / allocation failure.
+ */
+int xfa_oracle_head(const double *q, const double *k, const double *v, const double *dout,
+                    long S, long hd, double scale, int causal,
+                    double *out, double *lse, double *dq, double *dk, double *dv,
+                    double *p_rowsum, double *pdp_rowsum, double *ds_rowsum)
+{
+    return head_impl(q, k, v, dout, S, hd, scale, causal, NULL, out, lse, dq, dk, dv, p_rowsum, pdp_rowsum,
+                     ds_rowsum);
+}
+
+/*
+ * The same head with dropout of rate p (0 <= p < 1) on the attention
+ * probabilities; element (i, j) of this head has flat index index_base + i*S + j
+ * (index_base = b*S*S for head b of a [bh, S, S] probability tensor).
+ */
+int xfa_oracle_head_dropout(const double *q, const double *k, const double *v, const double *dout,
+                            long S, long hd, double scale, int causal, float p, uint64_t seed,
+                            uint64_t index_base, double *out, double *lse, double *dq, double *dk,
+                            double *dv, double *p_rowsum, double *pdp_rowsum, double *ds_rowsum)
+{
+    if (!(p >= 0.0f && p < 1.0f) || S < 1) return ORACLE_BAD_ARG;
+    double *C = (double *)malloc(sizeof(double) * (size_t)S * (size_t)S);
+    if (!C) return ORACLE_NO_MEMORY;
+    const double inv_keep = 1.0 / (1.0 - (double)p);
+    for (long i = 0; i < S; ++i)
+        for (long j = 0; j < S; ++j)
+            C[i * S + j] = xfa_oracle_keep(seed, index_base + (uint64_t)(i * S + j), p) ? inv_keep : 0.0;
+    const int rc = head_impl(q, k, v, dout, S, hd, scale, causal, C, out, lse, dq, dk, dv, p_rowsum, pdp_rowsum,
+                             ds_rowsum);
+    free(C);
+    return rc;
 }
 
 /* number of OpenMP threads the oracle runs with (1 when built without OpenMP) */

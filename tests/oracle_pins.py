@@ -163,3 +163,131 @@ def pin_finite_differences(head, cases=((5, 3, 1, True), (8, 4, 2, True), (6, 2,
 
 
 ALL_PINS = (pin_hand_2x2, pin_row_identities, pin_dense_library, pin_special_cases, pin_finite_differences)
+
+
+# ---------------------------------------------------------------- dropout on the probabilities
+# These take the oracle object (``oracle.Oracle``): besides ``head`` they use its
+# ``splitmix64`` and ``keep``.  The generator is the dropout page's ("xtrain
+# docs/17-dropout.md", section "Key Design Decisions"): key = seed ^ (idx * golden),
+# h = splitmix64(key), u = (h >> 40) / 2^24, keep = u >= p.
+
+GOLDEN_GAMMA = 0x9E3779B97F4A7C15
+
+# Outputs of the reference SplitMix64 generator (Steele, Lea, Flood 2014) started from
+# state 0: each step advances the state by the golden gamma and mixes it, so the n-th
+# output is splitmix64((n - 1) * gamma) in the one-step form the oracle exports.
+SPLITMIX64_FROM_ZERO = (0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F)
+
+
+def pin_dropout_generator_outputs(orc):
+    """The bit mix reproduces the published SplitMix64 outputs."""
+    for n, want in enumerate(SPLITMIX64_FROM_ZERO):
+        got = orc.splitmix64((n * GOLDEN_GAMMA) % 2 ** 64)
+        if got != want:
+            raise AssertionError(f"splitmix64 output {n}: {got:#x} != {want:#x}")
+
+
+def pin_dropout_keep_known_answers(orc):
+    """keep() against the page's definition worked by hand from the published outputs:
+    (seed, index) = (0, 0) gives key 0 and h = 0xE220A8397B1DCDAF, so u = 0xE220A8 / 2^24
+    = 0.883300...; (0, 1) gives key = gamma, h = 0x6E789E6AA1B965F4, u = 0.431528...;
+    (2 gamma, 0) gives key = 2 gamma, h = 0x06C45D188009454F, u = 0.026433...
+    Each element is kept for p just below its u and dropped for p just above."""
+    for seed, index, u in ((0, 0, 0.8833), (0, 1, 0.43153), ((2 * GOLDEN_GAMMA) % 2 ** 64, 0, 0.026433)):
+        if not orc.keep(seed, index, u - 1e-4) or orc.keep(seed, index, u + 1e-4):
+            raise AssertionError(f"keep({seed:#x}, {index}) does not switch at u = {u}")
+
+
+def pin_dropout_keep_rate(orc, n=1 << 15, seed=0xC0FFEE):
+    """Each element is kept with probability 1 - p: the kept fraction of n indices lies
+    within 6 standard deviations of 1 - p; p = 0 keeps everything."""
+    if not all(orc.keep(seed, i, 0.0) for i in range(0, n, 37)):
+        raise AssertionError("p = 0 dropped an element")
+    for p in (0.1, 0.5, 0.9):
+        kept = sum(orc.keep(seed, i, p) for i in range(n))
+        sd = math.sqrt(n * p * (1 - p))
+        if abs(kept - n * (1 - p)) > 6 * sd:
+            raise AssertionError(f"p={p}: kept {kept} of {n}, expected {n * (1 - p):.0f} +- {6 * sd:.0f}")
+
+
+def pin_dropout_p_zero(orc):
+    """Rate 0 is the plain operator, bit for bit."""
+    rng = np.random.default_rng(41)
+    S, hd = 9, 4
+    q, k, v, do = (_rand(rng, S, hd) for _ in range(4))
+    a = orc.head(q, k, v, do, 0.5, True)
+    b = orc.head(q, k, v, do, 0.5, True, dropout=(0.0, 77, 5 * S * S))
+    for n in a:
+        if not np.array_equal(a[n], b[n]):
+            raise AssertionError(f"p = 0 changed {n}")
+
+
+def pin_dropout_mask_structure(orc, S=6, p=0.4, seed=123, index_base=2 * 36):
+    """With V = I the output is P o C itself: every factor C_ij equals keep(seed,
+    index_base + i*S + j, p) / (1 - p) where P_ij > 0, and L is the plain L."""
+    rng = np.random.default_rng(5)
+    q, k = _rand(rng, S, S), _rand(rng, S, S)   # hd = S so that V can be the identity
+    v = np.eye(S)
+    plain = orc.head(q, k, v, None, 0.7, True)
+    drop = orc.head(q, k, v, None, 0.7, True, dropout=(p, seed, index_base))
+    _close(drop["lse"], plain["lse"], 0.0, "dropout changed L")
+    inv = 1.0 / (1.0 - np.float64(np.float32(p)))
+    for i in range(S):
+        for j in range(S):
+            c = inv if orc.keep(seed, index_base + i * S + j, p) else 0.0
+            _close(drop["out"][i, j], plain["out"][i, j] * c, 1e-15, f"factor ({i},{j})")
+
+
+def pin_dropout_finite_differences(orc, cases=((5, 3, 1), (7, 2, 2)), p=0.3, h=1e-6, rtol=2e-7):
+    """With the mask fixed (it depends on (seed, index) only), the gradients are the
+    central differences in fp64 of f = sum(dO o O)."""
+    for S, hd, seed in cases:
+        rng = np.random.default_rng(300 + seed)
+        x = {n: _rand(rng, S, hd) for n in ("q", "k", "v")}
+        do = _rand(rng, S, hd)
+        scale = 1.0 / math.sqrt(hd)
+        dd = (p, 1000 + seed, 3 * S * S)
+        r = orc.head(x["q"], x["k"], x["v"], do, scale, True, dropout=dd)
+
+        def f(**kw):
+            a = dict(x)
+            a.update(kw)
+            return float(np.sum(do * orc.head(a["q"], a["k"], a["v"], None, scale, True, dropout=dd)["out"]))
+
+        for n, gname in (("q", "dq"), ("k", "dk"), ("v", "dv")):
+            g = np.zeros((S, hd))
+            for i in range(S):
+                for d in range(hd):
+                    xp, xm = x[n].copy(), x[n].copy()
+                    xp[i, d] += h
+                    xm[i, d] -= h
+                    g[i, d] = (f(**{n: xp}) - f(**{n: xm})) / (2 * h)
+            tol = rtol * max(1.0, float(np.max(np.abs(g))))
+            _close(r[gname], g, tol, f"dropout FD {gname} S={S} hd={hd}")
+
+
+def pin_dropout_d_identity(orc, S=40, hd=8, p=0.25):
+    """The row term of the softmax backward still equals dO_i . O_i with dropout on
+    (sum_j P_ij dP_ij = sum_j (P o C)_ij (dO V^T)_ij = dO_i . O_i), which is what lets
+    the fused backward keep the D pre-pass unchanged."""
+    rng = np.random.default_rng(9)
+    q, k, v, do = (_rand(rng, S, hd) for _ in range(4))
+    r = orc.head(q, k, v, do, 1.0 / math.sqrt(hd), True, diagnostics=True, dropout=(p, 4, 0))
+    _close(r["pdp_rowsum"], np.sum(do * r["out"], axis=1), 1e-12, "sum_j P dP != dO . O with dropout")
+
+
+def pin_dropout_expectation(orc, S=5, hd=2, p=0.5, seeds=600):
+    """Inverted dropout keeps the expectation: over many seeds the mean output is the
+    plain output (within 6 standard errors of the sample mean)."""
+    rng = np.random.default_rng(17)
+    q, k, v = (_rand(rng, S, hd) for _ in range(3))
+    plain = orc.head(q, k, v, None, 0.8, True)["out"]
+    outs = np.stack([orc.head(q, k, v, None, 0.8, True, dropout=(p, s, 0))["out"] for s in range(seeds)])
+    mean, se = outs.mean(0), outs.std(0) / math.sqrt(seeds)
+    if np.any(np.abs(mean - plain) > 6 * se + 1e-12):
+        raise AssertionError(f"mean over seeds drifts: max |mean - plain| {np.max(np.abs(mean - plain)):.3e}")
+
+
+DROPOUT_PINS = (pin_dropout_generator_outputs, pin_dropout_keep_known_answers, pin_dropout_keep_rate, pin_dropout_p_zero,
+                pin_dropout_mask_structure, pin_dropout_finite_differences, pin_dropout_d_identity,
+                pin_dropout_expectation)

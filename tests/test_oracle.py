@@ -17,6 +17,11 @@ def test_oracle_pin(pin, head):
     pin(head)
 
 
+@pytest.mark.parametrize("pin", oracle_pins.DROPOUT_PINS, ids=lambda p: p.__name__)
+def test_oracle_dropout_pin(pin):
+    pin(oracle.default())
+
+
 def test_batched_matches_per_head():
     w = inputs.WORKLOADS[1]
     x = inputs.workload_inputs(w)

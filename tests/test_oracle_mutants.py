@@ -23,9 +23,17 @@ MUTANTS = {
     "scale dropped in backward": ("drow[j] = scale * (prow[j] * (drow[j] - dot));", "drow[j] = (prow[j] * (drow[j] - dot));"),
     "dQ uses Q instead of K": ("matmul_nn(dP, k, S, hd, dq);", "matmul_nn(dP, q, S, hd, dq);"),
     "dK not transposed": ("matmul_tn(dP, q, S, hd, dk);", "matmul_nn(dP, q, S, hd, dk);"),
-    "dV not transposed": ("matmul_tn(P, dout, S, hd, dv);", "matmul_nn(P, dout, S, hd, dv);"),
+    "dV not transposed": ("matmul_tn(C ? Pd : P, dout, S, hd, dv);", "matmul_nn(C ? Pd : P, dout, S, hd, dv);"),
     "dP operands swapped": ("matmul_nt(dout, v, S, hd, dP);", "matmul_nt(v, dout, S, hd, dP);"),
-    "O uses K instead of V": ("matmul_nn(P, v, S, hd, out);", "matmul_nn(P, k, S, hd, out);"),
+    "O uses K instead of V": ("matmul_nn(C ? Pd : P, v, S, hd, out);", "matmul_nn(C ? Pd : P, k, S, hd, out);"),
+    # dropout on the attention probabilities
+    "dropout mask missing in the backward": ("dP[e] *= C[e];", "dP[e] *= 1.0;"),
+    "dropout not inverted": ("? inv_keep : 0.0;", "? 1.0 : 0.0;"),
+    "dV from the undropped P": ("matmul_tn(C ? Pd : P, dout, S, hd, dv);", "matmul_tn(P, dout, S, hd, dv);"),
+    "dropout index transposed": ("index_base + (uint64_t)(i * S + j)", "index_base + (uint64_t)(j * S + i)"),
+    "keep test reversed": ("return u >= p;", "return u < p;"),
+    "keep from the low bits": ("(float)(h >> 40)", "(float)(h & 0xFFFFFF)"),
+    "bit-mix constant": ("z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;", "z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B8ull;"),
 }
 
 
@@ -36,11 +44,11 @@ def test_mutant_is_caught(name, tmp_path):
     old, new = MUTANTS[name]
     assert src.count(old) == 1, f"mutation anchor not found once: {old!r}"
     lib = oracle.compile_source(src.replace(old, new), str(tmp_path / "mutant.so"))
-    head = oracle.Oracle(lib).head
+    orc = oracle.Oracle(lib)
     failures = []
-    for pin in oracle_pins.ALL_PINS:
+    for pin, arg in [(p, orc.head) for p in oracle_pins.ALL_PINS] + [(p, orc) for p in oracle_pins.DROPOUT_PINS]:
         try:
-            pin(head)
+            pin(arg)
         except (AssertionError, FloatingPointError, RuntimeError) as e:
             failures.append(f"{pin.__name__}: {e}")
     assert failures, f"mutant '{name}' passed every pin"
