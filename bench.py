@@ -34,6 +34,7 @@ from bwd_xfa_fwd_gb300 import inputs  # noqa: E402
 METRIC = "causal attn fwd / bwd TFLOP/s at 1 GB300 and fraction of bf16 tensor peak"
 FAMILIES = {"auto": 0, "simt": 1, "tcgen05": 2, "tcgen05_det": 3}   # xfa_impl codes
 WORKLOAD_ID = 5
+DROPOUT_SEED = 0x5EED   # seed of the optional dropout mode (--dropout)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -284,6 +285,20 @@ def run_ours(args, w):
                 mark("finish", 1)
 
         mark("fwd", 0)
+        if args.dropout:
+            # dropout on the attention probabilities: the backward is one xfa_bwd_dropout call
+            # (its pre-pass, kernel and conversion), timed as "main"
+            binding.fwd(q, k, v, w.scale, impl, out=out, lse=lse, dropout_p=args.dropout, seed=DROPOUT_SEED)
+            mark("fwd", 1)
+            mark("prep", 0)
+            mark("prep", 1)
+            mark("main", 0)
+            binding.bwd(q, k, v, out, do, lse, w.scale, impl, workspace=ws, grads=grads, dropout_p=args.dropout,
+                        seed=DROPOUT_SEED)
+            mark("main", 1)
+            mark("finish", 0)
+            mark("finish", 1)
+            return
         binding.fwd(q, k, v, w.scale, impl, out=out, lse=lse)
         mark("fwd", 1)
         binding.bwd_stages(q, k, v, out, do, lse, w.scale, ws, grads, impl=impl, hook=hook)
@@ -320,7 +335,7 @@ def run_ours(args, w):
     # (upload, compute, download) with double-buffered device tensors, so step i's
     # compute overlaps step i+1's upload and step i-1's download.
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.dropout:
         e2e = measure_e2e(torch, binding, w, dev, ws, impl, K, f_fwd + f_bwd, world)
 
     pk, pk_kind = peaks()
@@ -341,7 +356,8 @@ def run_ours(args, w):
         "vs_baseline": None,
         "dtype": w.dtype,
         "data": "synthetic (seeded N(0,1), bf16-rounded; recipe in bwd_xfa_fwd_gb300/inputs.py)",
-        "config": dict(workload_config(w), kernel_family=args.family),
+        "config": dict(workload_config(w), kernel_family=args.family,
+                       **({"dropout_p": args.dropout, "dropout_seed": DROPOUT_SEED} if args.dropout else {})),
         "fwd_tflops": f_fwd / (per["fwd"] * 1e-3) / 1e12,
         "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
         "fwd_frac_of_peak": f_fwd / (per["fwd"] * 1e-3) / 1e12 / peak_tc,
@@ -349,18 +365,23 @@ def run_ours(args, w):
         "peak_bf16_tflops": peak_tc,
         "peak_kind": f"{pk_kind} burst bf16 dense (cuBLAS)",
         "stage_ms": per,
-        "roofline": {"kernel": fam.format("bwd") + " (xfa_bwd_main)", "bound": "tensor", "achieved": main_tflops,
+        "roofline": {"kernel": fam.format("bwd") + (" with its pre-pass and conversion (xfa_bwd_dropout)"
+                                                     if args.dropout else " (xfa_bwd_main)"),
+                     "bound": "tensor", "achieved": main_tflops,
                      "peak": peak_tc, "unit": "TFLOP/s", "frac": main_tflops / peak_tc,
-                     "traffic": recorded_traffic("tc_bwd", w.name) if w.dtype == "bf16" else None,
+                     "traffic": (recorded_traffic("tc_bwd", w.name) if w.dtype == "bf16" and not args.dropout
+                                 else None),
                      "peak_source": f"{pk_kind} bf16_tflops"},
         "roofline_fwd": {"kernel": fam.format("fwd") + " (xfa_fwd)", "bound": "tensor",
                          "achieved": f_fwd / (per["fwd"] * 1e-3) / 1e12, "peak": peak_tc, "unit": "TFLOP/s",
                          "frac": f_fwd / (per["fwd"] * 1e-3) / 1e12 / peak_tc,
-                         "traffic": recorded_traffic("tc_fwd", w.name) if w.dtype == "bf16" else None},
-        "roofline_prep": {"kernel": "rowdot_kernel (xfa_bwd_prep)", "bound": "hbm",
-                          "achieved": prep_bytes / (per["prep"] * 1e-3) / 1e9, "peak": float(pk["hbm_gbs"]),
-                          "unit": "GB/s", "frac": prep_bytes / (per["prep"] * 1e-3) / 1e9 / float(pk["hbm_gbs"]),
-                          "traffic": recorded_traffic("rowdot", w.name)},
+                         "traffic": (recorded_traffic("tc_fwd", w.name) if w.dtype == "bf16" and not args.dropout
+                                     else None)},
+        "roofline_prep": None if args.dropout else {
+            "kernel": "rowdot_kernel (xfa_bwd_prep)", "bound": "hbm",
+            "achieved": prep_bytes / (per["prep"] * 1e-3) / 1e9, "peak": float(pk["hbm_gbs"]),
+            "unit": "GB/s", "frac": prep_bytes / (per["prep"] * 1e-3) / 1e9 / float(pk["hbm_gbs"]),
+            "traffic": recorded_traffic("rowdot", w.name)},
         "e2e": e2e,
         "gpu_launches": 4 * K,
         "clocks": clk.result,
@@ -383,6 +404,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--dropout", type=float, default=0.0,
+                    help="dropout rate on the attention probabilities (0: none, the benchmark's default)")
     ap.add_argument("--family", choices=sorted(FAMILIES), default="auto",
                     help="kernel family (xfa_impl): auto, tcgen05 (dQ by fp32 reductions), "
                          "tcgen05_det (dQ by a separate pass, bit-reproducible), simt")

@@ -37,13 +37,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: build it with bwd_xfa_fwd_gb300.build.build()")
     lib = ctypes.CDLL(path)
-    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    vp, i, f, sz, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_ulonglong
     sigs = {
         "xfa_fwd": ([vp, vp, vp, vp, vp, i, i, i, f, i, vp], i),
         "xfa_fwd_impl": ([vp, vp, vp, vp, vp, i, i, i, f, i, i, vp], i),
+        "xfa_fwd_dropout": ([vp, vp, vp, vp, vp, i, i, i, f, i, f, u64, i, vp], i),
         "xfa_bwd_workspace_bytes": ([i, i, i, i], sz),
         "xfa_bwd": ([vp] * 9 + [i, i, i, f, i, vp, sz, vp], i),
         "xfa_bwd_impl": ([vp] * 9 + [i, i, i, f, i, vp, sz, i, vp], i),
+        "xfa_bwd_dropout": ([vp] * 9 + [i, i, i, f, i, f, u64, vp, sz, i, vp], i),
         "xfa_bwd_prep": ([vp, vp, vp, vp, i, i, i, i, vp, sz, i, vp], i),
         "xfa_bwd_main": ([vp] * 7 + [i, i, i, f, i, vp, sz, i, vp], i),
         "xfa_bwd_finish": ([vp, i, i, i, i, vp, sz, i, vp], i),
@@ -101,15 +103,22 @@ def default_scale(hd: int) -> float:
     return 1.0 / math.sqrt(hd)
 
 
-def fwd(q, k, v, scale: float | None = None, impl: int = IMPL_AUTO, out=None, lse=None):
-    """Forward: returns (O, L).  O has q's shape/dtype; L is fp32 [..., S]."""
+def fwd(q, k, v, scale: float | None = None, impl: int = IMPL_AUTO, out=None, lse=None, dropout_p: float = 0.0,
+        seed: int = 0):
+    """Forward: returns (O, L).  O has q's shape/dtype; L is fp32 [..., S].  ``dropout_p`` > 0
+    applies dropout of that rate to the attention probabilities (xfa_fwd_dropout); the
+    backward must get the same ``dropout_p`` and ``seed``."""
     _check_tensors(q, k, v)
     bh, S, hd = _shape3(q)
     scale = default_scale(hd) if scale is None else float(scale)
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty(q.shape[:-1], device=q.device, dtype=torch.float32) if lse is None else lse
-    _check(load().xfa_fwd_impl(_p(q), _p(k), _p(v), _p(out), _p(lse), bh, S, hd, scale, _DTYPE[q.dtype], impl,
-                               _stream(q)), "xfa_fwd")
+    if dropout_p:
+        _check(load().xfa_fwd_dropout(_p(q), _p(k), _p(v), _p(out), _p(lse), bh, S, hd, scale, _DTYPE[q.dtype],
+                                      float(dropout_p), int(seed) % 2 ** 64, impl, _stream(q)), "xfa_fwd_dropout")
+    else:
+        _check(load().xfa_fwd_impl(_p(q), _p(k), _p(v), _p(out), _p(lse), bh, S, hd, scale, _DTYPE[q.dtype], impl,
+                                   _stream(q)), "xfa_fwd")
     return out, lse
 
 
@@ -117,8 +126,10 @@ def workspace_bytes(bh: int, S: int, hd: int, dtype: torch.dtype) -> int:
     return int(load().xfa_bwd_workspace_bytes(bh, S, hd, _DTYPE[dtype]))
 
 
-def bwd(q, k, v, out, dout, lse, scale: float | None = None, impl: int = IMPL_AUTO, workspace=None, grads=None):
-    """Backward: returns (dQ, dK, dV), each of q's shape/dtype (overwritten)."""
+def bwd(q, k, v, out, dout, lse, scale: float | None = None, impl: int = IMPL_AUTO, workspace=None, grads=None,
+        dropout_p: float = 0.0, seed: int = 0):
+    """Backward: returns (dQ, dK, dV), each of q's shape/dtype (overwritten).  ``dropout_p`` and
+    ``seed`` must be those of the forward (xfa_bwd_dropout when ``dropout_p`` > 0)."""
     _check_tensors(q, k, v, out, dout)
     bh, S, hd = _shape3(q)
     scale = default_scale(hd) if scale is None else float(scale)
@@ -126,9 +137,14 @@ def bwd(q, k, v, out, dout, lse, scale: float | None = None, impl: int = IMPL_AU
     if workspace is None:
         workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
     dq, dk, dv = grads if grads is not None else (torch.empty_like(q), torch.empty_like(q), torch.empty_like(q))
-    _check(load().xfa_bwd_impl(_p(q), _p(k), _p(v), _p(out), _p(dout), _p(lse), _p(dq), _p(dk), _p(dv), bh, S, hd,
-                               scale, _DTYPE[q.dtype], _p(workspace), workspace.numel(), impl, _stream(q)),
-           "xfa_bwd")
+    if dropout_p:
+        _check(load().xfa_bwd_dropout(_p(q), _p(k), _p(v), _p(out), _p(dout), _p(lse), _p(dq), _p(dk), _p(dv), bh, S,
+                                      hd, scale, _DTYPE[q.dtype], float(dropout_p), int(seed) % 2 ** 64,
+                                      _p(workspace), workspace.numel(), impl, _stream(q)), "xfa_bwd_dropout")
+    else:
+        _check(load().xfa_bwd_impl(_p(q), _p(k), _p(v), _p(out), _p(dout), _p(lse), _p(dq), _p(dk), _p(dv), bh, S,
+                                   hd, scale, _DTYPE[q.dtype], _p(workspace), workspace.numel(), impl, _stream(q)),
+               "xfa_bwd")
     return dq, dk, dv
 
 

@@ -3,11 +3,24 @@
 #pragma once
 
 #include <cstddef>
+#include <cstdint>
+
 #include <cuda_runtime.h>
 
 #include "xfa.h"
 
 namespace xfa {
+
+// Dropout on the attention probabilities (see dropout.cuh): element (b, i, j) of the
+// [bh, S, S] probabilities is kept when the 24-bit draw of its flat index is >= keep_thr
+// (= ceil(p * 2^24), so the test equals u = draw / 2^24 >= p exactly) and then scaled by
+// inv_keep = 1 / (1 - p).  on == false: no dropout (the plain kernels run).
+struct DropParams {
+    bool on = false;
+    uint32_t keep_thr = 0;
+    float inv_keep = 1.0f;
+    uint64_t seed = 0;
+};
 
 struct FwdParams {
     const void *q, *k, *v;
@@ -17,6 +30,7 @@ struct FwdParams {
     float scale;
     int dtype;
     int *status;   // device status word
+    DropParams drop;
 };
 
 struct BwdParams {
@@ -32,6 +46,7 @@ struct BwdParams {
     float *dq_acc;  // [bh][S][hd]  fp32 dQ accumulator (== dq when dtype is fp32)
     int S_pad;
     int *status;
+    DropParams drop;
 };
 
 // Rows of D / Lg are padded to a multiple of this.

@@ -19,6 +19,7 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include "dropout.cuh"
 #include "kernels.h"
 
 namespace xfa {
@@ -49,10 +50,11 @@ __device__ __forceinline__ void load_tile(float *dst, int pitch, const T *src, i
     }
 }
 
-template <typename T, int HD>
+template <typename T, int HD, bool DROP>
 __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(const T *__restrict__ Q, const T *__restrict__ K,
                                                            const T *__restrict__ V, T *__restrict__ O,
-                                                           float *__restrict__ lse, int S, float scale_log2)
+                                                           float *__restrict__ lse, int S, float scale_log2,
+                                                           const DropParams drop)
 {
     extern __shared__ float smem[];
     constexpr int KP = HD + 1;        // padded pitch for K (column walks)
@@ -132,11 +134,20 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(const T *__restrict_
             const float m_old = m_s[r];
             const float m_new = fmaxf(m_old, mx);
             float sum = 0.0f;
+            // dropout: the P.V product takes p o C (C_ij = keep / (1 - p)); the row sum keeps every p
+            const uint64_t drop_g =
+                DROP ? (((uint64_t)head * S + (uint64_t)(q0 + r)) * (uint64_t)S + (uint64_t)(k0 + part * 16)) *
+                           kDropGolden
+                     : 0ull;
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 const float p = exp2f(prow[c] - m_new);
-                prow[c] = p;
                 sum += p;
+                if (DROP)
+                    prow[c] = drop_keep(drop.seed, drop_g + (uint64_t)c * kDropGolden, drop.keep_thr) ? p * drop.inv_keep
+                                                                                                     : 0.0f;
+                else
+                    prow[c] = p;
             }
             sum += __shfl_xor_sync(0xffffffffu, sum, 1);
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
@@ -174,13 +185,13 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(const T *__restrict_
     }
 }
 
-template <typename T, int HD>
+template <typename T, int HD, bool DROP>
 __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(const T *__restrict__ Q, const T *__restrict__ K,
                                                            const T *__restrict__ V, const T *__restrict__ dO,
                                                            const float *__restrict__ Lg, const float *__restrict__ Dv,
                                                            float *__restrict__ dQacc, T *__restrict__ dK,
                                                            T *__restrict__ dV, int S, int S_pad, float scale,
-                                                           float scale_log2)
+                                                           float scale_log2, const DropParams drop)
 {
     extern __shared__ float smem[];
     constexpr int P = HD + 1;
@@ -254,8 +265,16 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(const T *__restrict_
                 const int r = sr0 + i, c = sc + 16 * j;
                 const bool masked = (k0 + c) > (q0 + r);
                 const float p = masked ? 0.0f : exp2f(fmaf(s[i][j], scale_log2, Ls[r]));
-                Ps[r * (kTile + 1) + c] = p;
-                dSs[r * (kTile + 1) + c] = p * (dp[i][j] - Ds[r]) * scale;
+                if (DROP) {   // dV takes P o C; dS is formed from C o dP (the dropout node's backward)
+                    const uint64_t g =
+                        (((uint64_t)head * S + (uint64_t)(q0 + r)) * (uint64_t)S + (uint64_t)(k0 + c)) * kDropGolden;
+                    const bool keep = drop_keep(drop.seed, g, drop.keep_thr);
+                    Ps[r * (kTile + 1) + c] = keep ? p * drop.inv_keep : 0.0f;
+                    dSs[r * (kTile + 1) + c] = p * ((keep ? dp[i][j] * drop.inv_keep : 0.0f) - Ds[r]) * scale;
+                } else {
+                    Ps[r * (kTile + 1) + c] = p;
+                    dSs[r * (kTile + 1) + c] = p * (dp[i][j] - Ds[r]) * scale;
+                }
             }
         __syncthreads();
 
@@ -304,32 +323,32 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(const T *__restrict_
     }
 }
 
-template <typename T, int HD>
+template <typename T, int HD, bool DROP>
 cudaError_t run_fwd(const FwdParams &p, cudaStream_t st)
 {
     constexpr size_t smem = sizeof(float) * (kTile * HD * 2 + kTile * (HD + 1) + kTile * (kTile + 1) + 3 * kTile);
-    auto kern = simt_fwd_kernel<T, HD>;
+    auto kern = simt_fwd_kernel<T, HD, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int ntiles = (p.S + kTile - 1) / kTile;
     const unsigned grid = (unsigned)(ntiles * p.bh);
     kern<<<grid, kThreads, smem, st>>>((const T *)p.q, (const T *)p.k, (const T *)p.v, (T *)p.out, p.lse, p.S,
-                                       p.scale * kLog2e);
+                                       p.scale * kLog2e, p.drop);
     return cudaGetLastError();
 }
 
-template <typename T, int HD>
+template <typename T, int HD, bool DROP>
 cudaError_t run_bwd(const BwdParams &p, cudaStream_t st)
 {
     constexpr size_t smem = sizeof(float) * (4 * kTile * (HD + 1) + 2 * kTile * (kTile + 1) + 2 * kTile);
-    auto kern = simt_bwd_kernel<T, HD>;
+    auto kern = simt_bwd_kernel<T, HD, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int ntiles = (p.S + kTile - 1) / kTile;
     const unsigned grid = (unsigned)(ntiles * p.bh);
     kern<<<grid, kThreads, smem, st>>>((const T *)p.q, (const T *)p.k, (const T *)p.v, (const T *)p.dout, p.Lg,
                                        p.D, p.dq_acc, (T *)p.dk, (T *)p.dv, p.S, p.S_pad, p.scale,
-                                       p.scale * kLog2e);
+                                       p.scale * kLog2e, p.drop);
     return cudaGetLastError();
 }
 
@@ -337,9 +356,9 @@ template <typename T>
 cudaError_t fwd_dispatch(const FwdParams &p, cudaStream_t st)
 {
     switch (p.hd) {
-    case 32: return run_fwd<T, 32>(p, st);
-    case 64: return run_fwd<T, 64>(p, st);
-    case 128: return run_fwd<T, 128>(p, st);
+    case 32: return p.drop.on ? run_fwd<T, 32, true>(p, st) : run_fwd<T, 32, false>(p, st);
+    case 64: return p.drop.on ? run_fwd<T, 64, true>(p, st) : run_fwd<T, 64, false>(p, st);
+    case 128: return p.drop.on ? run_fwd<T, 128, true>(p, st) : run_fwd<T, 128, false>(p, st);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -348,9 +367,9 @@ template <typename T>
 cudaError_t bwd_dispatch(const BwdParams &p, cudaStream_t st)
 {
     switch (p.hd) {
-    case 32: return run_bwd<T, 32>(p, st);
-    case 64: return run_bwd<T, 64>(p, st);
-    case 128: return run_bwd<T, 128>(p, st);
+    case 32: return p.drop.on ? run_bwd<T, 32, true>(p, st) : run_bwd<T, 32, false>(p, st);
+    case 64: return p.drop.on ? run_bwd<T, 64, true>(p, st) : run_bwd<T, 64, false>(p, st);
+    case 128: return p.drop.on ? run_bwd<T, 128, true>(p, st) : run_bwd<T, 128, false>(p, st);
     default: return cudaErrorInvalidValue;
     }
 }

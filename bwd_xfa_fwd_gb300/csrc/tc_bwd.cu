@@ -32,6 +32,7 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include "dropout.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -160,14 +161,16 @@ __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t k_tmem, uint64
 
 // FUSED_DQ: dQ^T is formed here and summed into the fp32 accumulator (bulk reduce-add);
 // otherwise dQ is left to the query-tile pass (tc_dq.cu) and this kernel does dK, dV only.
-template <int HD, bool FUSED_DQ>
+// DROP: dropout on the attention probabilities (fused only): dV takes P o C and dS is
+// formed from C o dP, with C re-drawn from (seed, flat index).
+template <int HD, bool FUSED_DQ, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                   const float *__restrict__ Lg, const float *__restrict__ Dg, float *__restrict__ dq_acc,
                   __nv_bfloat16 *__restrict__ dK, __nv_bfloat16 *__restrict__ dV, int bh, int S, int S_pad,
-                  float scale, float scale_log2, int *status)
+                  float scale, float scale_log2, int *status, const DropParams drop)
 {
     using C = Cfg<HD>;
     constexpr int NSQ = C::NSQ;
@@ -391,6 +394,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t cs2 = f2_pack(scale_log2, scale_log2);
             const bool diag = key > i0;   // some (key > row) pairs in this tile
             uint64_t pp[32];              // P pairs (fp32) kept for dS
+            // dropout: element (row i0 + c, key) has flat index (head*S + i0 + c)*S + key; its index times
+            // the golden ratio steps by S * golden per column.  Keep bits of the 64 columns in km.
+            uint32_t km[2] = {0u, 0u};
+            uint64_t drop_g = DROP ? (((uint64_t)head * S + (uint64_t)i0) * (uint64_t)S + (uint64_t)key) * kDropGolden
+                                   : 0ull;
+            const uint64_t drop_step = DROP ? (uint64_t)S * kDropGolden : 0ull;
             {
                 uint32_t pk[32];
 #pragma unroll
@@ -407,7 +416,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (key > i0 + cc + 1) p1 = 0.0f;
                         }
                         pp[cc / 2] = f2_pack(p0, p1);
-                        pk[cc / 2] = pack_bf16x2(p0, p1);
+                        if (DROP) {
+                            const bool k0 = drop_keep(drop.seed, drop_g, drop.keep_thr);
+                            const bool k1 = drop_keep(drop.seed, drop_g + drop_step, drop.keep_thr);
+                            drop_g += 2 * drop_step;
+                            km[cc / 32] |= ((uint32_t)k0 << (cc % 32)) | ((uint32_t)k1 << (cc % 32 + 1));
+                            pk[cc / 2] = pack_bf16x2(k0 ? p0 * drop.inv_keep : 0.0f, k1 ? p1 * drop.inv_keep : 0.0f);
+                        } else {
+                            pk[cc / 2] = pack_bf16x2(p0, p1);
+                        }
                     }
                 }
                 tmem_st32(tmem + lane_off + C::COL_S, pk);
@@ -435,7 +452,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 16; ++e) {
                     const int c = 32 * h + 2 * e;
                     const float2 d2 = *reinterpret_cast<const float2 *>(Ds + c);
-                    const uint64_t t = ffma2(f2_pack(d2.x, d2.y), m1, f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])));
+                    float dp0 = __uint_as_float(dp[2 * e]), dp1 = __uint_as_float(dp[2 * e + 1]);
+                    if (DROP) {   // the dropout node's backward: dP = C o (dO V^T)
+                        dp0 = (km[c / 32] >> (c % 32)) & 1u ? dp0 * drop.inv_keep : 0.0f;
+                        dp1 = (km[c / 32] >> (c % 32 + 1)) & 1u ? dp1 * drop.inv_keep : 0.0f;
+                    }
+                    const uint64_t t = ffma2(f2_pack(d2.x, d2.y), m1, f2_pack(dp0, dp1));
                     const float2 ds = f2_unpack(fmul2(fmul2(pp[c / 2], sc2), t));
                     pk[e] = pack_bf16x2(ds.x, ds.y);
                 }
@@ -519,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int HD, bool FUSED_DQ>
+template <int HD, bool FUSED_DQ, bool DROP>
 int run(const BwdParams &p, cudaStream_t st)
 {
     alignas(64) CUtensorMap tk, tv, tq, tdo, tdk, tdv;
@@ -532,14 +554,14 @@ int run(const BwdParams &p, cudaStream_t st)
     if (rc != XFA_OK) return rc;
     static_assert(Cfg<HD>::SMEM <= 227 * 1024, "shared memory per CTA");
     static_assert(Cfg<HD>::NSQ * Cfg<HD>::Q_BYTES >= Cfg<HD>::KV_BYTES, "dK / dV staging fits a ring");
-    auto kern = tc_bwd_kernel<HD, FUSED_DQ>;
+    auto kern = tc_bwd_kernel<HD, FUSED_DQ, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<HD>::SMEM);
     if (e != cudaSuccess) return XFA_ERR_CUDA_BASE + (int)e;
     const int nkt = (p.S + BN - 1) / BN;
     const unsigned grid = (unsigned)(nkt * p.bh);
     kern<<<grid, kThreads, Cfg<HD>::SMEM, st>>>(tk, tv, tq, tdo, tdk, tdv, p.Lg, p.D, p.dq_acc, (__nv_bfloat16 *)p.dk,
                                                  (__nv_bfloat16 *)p.dv, p.bh, p.S, p.S_pad, p.scale,
-                                                 p.scale * 1.4426950408889634f, p.status);
+                                                 p.scale * 1.4426950408889634f, p.status, p.drop);
     e = cudaGetLastError();
     return e == cudaSuccess ? XFA_OK : XFA_ERR_CUDA_BASE + (int)e;
 }
@@ -549,8 +571,15 @@ int run(const BwdParams &p, cudaStream_t st)
 int launch_tc_bwd(const BwdParams &p, cudaStream_t st, bool fused_dq)
 {
     if (p.dtype != XFA_BF16) return XFA_ERR_UNSUPPORTED;
-    if (p.hd == 128) return fused_dq ? run<128, true>(p, st) : run<128, false>(p, st);
-    if (p.hd == 64) return fused_dq ? run<64, true>(p, st) : run<64, false>(p, st);
+    if (p.drop.on && !fused_dq) return XFA_ERR_UNSUPPORTED;   // dropout: fused variant only
+    if (p.hd == 128) {
+        if (p.drop.on) return run<128, true, true>(p, st);
+        return fused_dq ? run<128, true, false>(p, st) : run<128, false, false>(p, st);
+    }
+    if (p.hd == 64) {
+        if (p.drop.on) return run<64, true, true>(p, st);
+        return fused_dq ? run<64, true, false>(p, st) : run<64, false, false>(p, st);
+    }
     return XFA_ERR_UNSUPPORTED;
 }
 

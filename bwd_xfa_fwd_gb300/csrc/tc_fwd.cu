@@ -26,6 +26,7 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include "dropout.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -106,11 +107,12 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
         mma_ts(o_tmem, p_tmem + ks * 8, sdesc_advance(v_desc, ks * 2048), idesc, (accumulate || ks > 0) ? 1u : 0u);
 }
 
-template <int HD>
+// DROP: dropout on the probabilities that enter P.V (the row sums l keep every p).
+template <int HD, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ O,
-                  float *__restrict__ lse, int bh, int S, float scale_log2, int *status)
+                  float *__restrict__ lse, int bh, int S, float scale_log2, int *status, const DropParams drop)
 {
     using C = Cfg<HD>;
     extern __shared__ uint8_t smem_raw[];
@@ -272,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_off + C::col_o(t);
         float m = -CUDART_INF_F, l = 0.0f;
         bool ok = true;
+        const uint64_t drop_row_g = DROP ? ((uint64_t)head * S + (uint64_t)row) * (uint64_t)S * kDropGolden : 0ull;
         const int n_mine = t == 0 ? n_t0 : n_t1;
         for (int j = 0; j < n_mine; ++j) {
             if (!(ok = warp_wait(&bars->s_full[t], j & 1, bars, status))) break;
@@ -340,7 +343,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float p0 = ex2_approx(a.x);
                     const float p1 = ex2_approx(a.y);
                     l2[e & 3] = fadd2(l2[e & 3], f2_pack(p0, p1));
-                    pk[e] = pack_bf16x2(p0, p1);
+                    if (DROP) {
+                        // keys j*BN + c, c + 1 of this row: flat index (head*S + row)*S + key
+                        const uint64_t g0 = drop_row_g + (uint64_t)(j * BN + c) * kDropGolden;
+                        const float d0 = drop_keep(drop.seed, g0, drop.keep_thr) ? p0 * drop.inv_keep : 0.0f;
+                        const float d1 =
+                            drop_keep(drop.seed, g0 + kDropGolden, drop.keep_thr) ? p1 * drop.inv_keep : 0.0f;
+                        pk[e] = pack_bf16x2(d0, d1);
+                    } else {
+                        pk[e] = pack_bf16x2(p0, p1);
+                    }
                 }
                 tmem_st32(tS + 32 * h, pk);
             }
@@ -388,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int HD>
+template <int HD, bool DROP>
 int run(const FwdParams &p, cudaStream_t st)
 {
     alignas(64) CUtensorMap tq, tk, tv;
@@ -397,13 +409,13 @@ int run(const FwdParams &p, cudaStream_t st)
     if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tv, p.v, HD, p.S, p.bh, BN);
     if (rc != XFA_OK) return rc;
     static_assert(Cfg<HD>::SMEM <= 227 * 1024, "shared memory per CTA");
-    auto kern = tc_fwd_kernel<HD>;
+    auto kern = tc_fwd_kernel<HD, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<HD>::SMEM);
     if (e != cudaSuccess) return XFA_ERR_CUDA_BASE + (int)e;
     const int nqb = (p.S + 2 * BM - 1) / (2 * BM);
     const unsigned grid = (unsigned)(nqb * p.bh);
     kern<<<grid, kThreads, Cfg<HD>::SMEM, st>>>(tq, tk, tv, (__nv_bfloat16 *)p.out, p.lse, p.bh, p.S,
-                                                 p.scale * 1.4426950408889634f, p.status);
+                                                 p.scale * 1.4426950408889634f, p.status, p.drop);
     e = cudaGetLastError();
     return e == cudaSuccess ? XFA_OK : XFA_ERR_CUDA_BASE + (int)e;
 }
@@ -413,8 +425,8 @@ int run(const FwdParams &p, cudaStream_t st)
 int launch_tc_fwd(const FwdParams &p, cudaStream_t st)
 {
     if (p.dtype != XFA_BF16) return XFA_ERR_UNSUPPORTED;
-    if (p.hd == 128) return run<128>(p, st);
-    if (p.hd == 64) return run<64>(p, st);
+    if (p.hd == 128) return p.drop.on ? run<128, true>(p, st) : run<128, false>(p, st);
+    if (p.hd == 64) return p.drop.on ? run<64, true>(p, st) : run<64, false>(p, st);
     return XFA_ERR_UNSUPPORTED;
 }
 

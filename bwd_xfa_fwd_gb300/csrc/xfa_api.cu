@@ -179,8 +179,23 @@ const char *xfa_strerror(int code)
     return "unknown error";
 }
 
-int xfa_fwd_impl(const void *q, const void *k, const void *v, void *out, float *lse, int bh, int S, int hd,
-                 float scale, int dtype, int impl, void *stream)
+}  // extern "C"
+
+// Dropout parameters of a call: rate p in [0, 1) (NaN rejected); p == 0 leaves dropout off.
+static int make_drop(float p, unsigned long long seed, DropParams *d)
+{
+    if (!(p >= 0.0f && p < 1.0f)) return XFA_ERR_INVALID_ARG;
+    *d = DropParams{};
+    if (p == 0.0f) return XFA_OK;
+    d->on = true;
+    d->keep_thr = (uint32_t)ceil((double)p * 16777216.0);   // u = draw / 2^24 >= p  <=>  draw >= keep_thr
+    d->inv_keep = (float)(1.0 / (1.0 - (double)p));
+    d->seed = seed;
+    return XFA_OK;
+}
+
+static int fwd_run(const void *q, const void *k, const void *v, void *out, float *lse, int bh, int S, int hd,
+                   float scale, int dtype, const DropParams &drop, int impl, void *stream)
 {
     int rc = validate_shape(bh, S, hd, scale, dtype);
     if (rc != XFA_OK) return rc;
@@ -189,10 +204,28 @@ int xfa_fwd_impl(const void *q, const void *k, const void *v, void *out, float *
     Family fam;
     if ((rc = choose_impl(impl, hd, dtype, &fam)) != XFA_OK) return rc;
     FwdParams p{q, k, v, out, lse, bh, S, hd, scale, dtype, nullptr};
+    p.drop = drop;
     if ((rc = status_ptr(&p.status)) != XFA_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (fam != Family::Simt) return launch_tc_fwd(p, st);
     return cuda_code(launch_simt_fwd(p, st));
+}
+
+extern "C" {
+
+int xfa_fwd_impl(const void *q, const void *k, const void *v, void *out, float *lse, int bh, int S, int hd,
+                 float scale, int dtype, int impl, void *stream)
+{
+    return fwd_run(q, k, v, out, lse, bh, S, hd, scale, dtype, DropParams{}, impl, stream);
+}
+
+int xfa_fwd_dropout(const void *q, const void *k, const void *v, void *out, float *lse, int bh, int S, int hd,
+                    float scale, int dtype, float p_drop, unsigned long long seed, int impl, void *stream)
+{
+    DropParams d;
+    const int rc = make_drop(p_drop, seed, &d);
+    if (rc != XFA_OK) return rc;
+    return fwd_run(q, k, v, out, lse, bh, S, hd, scale, dtype, d, impl, stream);
 }
 
 int xfa_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int bh, int S, int hd, float scale,
@@ -298,19 +331,45 @@ int xfa_bwd_finish(void *dq, int bh, int S, int hd, int dtype, void *workspace, 
     return stage_finish(p, fam, static_cast<cudaStream_t>(stream));
 }
 
-int xfa_bwd_impl(const void *q, const void *k, const void *v, const void *out, const void *dout, const float *lse,
-                 void *dq, void *dk, void *dv, int bh, int S, int hd, float scale, int dtype, void *workspace,
-                 size_t workspace_bytes, int impl, void *stream)
+}  // extern "C"
+
+static int bwd_run(const void *q, const void *k, const void *v, const void *out, const void *dout, const float *lse,
+                   void *dq, void *dk, void *dv, int bh, int S, int hd, float scale, int dtype, void *workspace,
+                   size_t workspace_bytes, const DropParams &drop, int impl, void *stream)
 {
     BwdParams p;
     int rc = bwd_setup(p, q, k, v, out, dout, lse, dq, dk, dv, bh, S, hd, scale, dtype, workspace, workspace_bytes);
     if (rc != XFA_OK) return rc;
+    p.drop = drop;
     Family fam;
     if ((rc = choose_impl(impl, hd, dtype, &fam)) != XFA_OK) return rc;
+    if (drop.on && fam == Family::TcDet) return XFA_ERR_UNSUPPORTED;   // dropout: fused and SIMT families only
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if ((rc = stage_prep(p, fam, st)) != XFA_OK) return rc;
     if ((rc = stage_main(p, fam, st)) != XFA_OK) return rc;
     return stage_finish(p, fam, st);
+}
+
+extern "C" {
+
+int xfa_bwd_impl(const void *q, const void *k, const void *v, const void *out, const void *dout, const float *lse,
+                 void *dq, void *dk, void *dv, int bh, int S, int hd, float scale, int dtype, void *workspace,
+                 size_t workspace_bytes, int impl, void *stream)
+{
+    return bwd_run(q, k, v, out, dout, lse, dq, dk, dv, bh, S, hd, scale, dtype, workspace, workspace_bytes,
+                   DropParams{}, impl, stream);
+}
+
+int xfa_bwd_dropout(const void *q, const void *k, const void *v, const void *out, const void *dout,
+                    const float *lse, void *dq, void *dk, void *dv, int bh, int S, int hd, float scale, int dtype,
+                    float p_drop, unsigned long long seed, void *workspace, size_t workspace_bytes, int impl,
+                    void *stream)
+{
+    DropParams d;
+    const int rc = make_drop(p_drop, seed, &d);
+    if (rc != XFA_OK) return rc;
+    return bwd_run(q, k, v, out, dout, lse, dq, dk, dv, bh, S, hd, scale, dtype, workspace, workspace_bytes, d, impl,
+                   stream);
 }
 
 int xfa_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout, const float *lse,

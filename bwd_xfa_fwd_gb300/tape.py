@@ -80,17 +80,21 @@ class Var:
         return f"Var(shape={tuple(self.value.shape)}, dtype={self.value.dtype}, leaf={self.backward_fn is None})"
 
 
-def flash_attention(q: Var, k: Var, v: Var, scale: Optional[float] = None, impl: int = 0) -> Var:
-    """Causal flash attention as one tape node: returns Var(O); caches L."""
+def flash_attention(q: Var, k: Var, v: Var, scale: Optional[float] = None, impl: int = 0, dropout_p: float = 0.0,
+                    seed: int = 0) -> Var:
+    """Causal flash attention as one tape node: returns Var(O); caches L.  ``dropout_p`` > 0
+    drops attention probabilities with the counter-based mask of ``seed``; the backward
+    re-draws the same mask (nothing but the seed is kept)."""
     from . import binding
 
-    out, lse = binding.fwd(q.value, k.value, v.value, scale, impl)
+    out, lse = binding.fwd(q.value, k.value, v.value, scale, impl, dropout_p=dropout_p, seed=seed)
     hd = q.value.shape[-1]
     sc = binding.default_scale(hd) if scale is None else float(scale)
 
     def backward_fn(grad, parents):
         pq, pk, pv = parents
-        dq, dk, dv = binding.bwd(pq.value, pk.value, pv.value, out, grad.contiguous(), lse, sc, impl)
+        dq, dk, dv = binding.bwd(pq.value, pk.value, pv.value, out, grad.contiguous(), lse, sc, impl,
+                                 dropout_p=dropout_p, seed=seed)
         pq.accumulate(dq)
         pk.accumulate(dk)
         pv.accumulate(dv)

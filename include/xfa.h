@@ -122,6 +122,36 @@ int xfa_bwd_impl(const void *q, const void *k, const void *v, const void *out, c
                  void *workspace, size_t workspace_bytes, int impl, void *stream);
 
 /*
+ * Forward and backward with dropout on the attention probabilities.  Passage:
+ * "xtrain docs/17-dropout.md", section "Key Design Decisions" (counter-based
+ * draw: key = seed XOR (idx * 0x9E3779B97F4A7C15), h = splitmix64(key),
+ * u = (h >> 40) / 2^24, keep = u >= p; kept elements scaled by 1 / (1 - p);
+ * the backward re-draws the same mask from (seed, idx)).  The page applies it to
+ * activations and leaves the attention probabilities out; here it sits between
+ * the softmax and the product with V:
+ *   O_i = sum_j P_ij C_ij V_j,   C_ij = keep(seed, (b*S + i)*S + j) / (1 - p),
+ * L is the plain logsumexp (the softmax is unchanged), and the backward uses
+ * dP_ij = C_ij dO_i . V_j in place of dO_i . V_j (D_i = dO_i . O_i still holds).
+ *   p_drop : rate in [0, 1); anything else (or NaN) gives XFA_ERR_INVALID_ARG.
+ *            p_drop == 0 runs the plain kernels (results bit for bit those of
+ *            xfa_fwd_impl / xfa_bwd_impl).
+ *   seed   : 64-bit seed; the forward and the backward of one use must get the
+ *            same seed and p_drop.
+ * Other arguments as xfa_fwd_impl / xfa_bwd_impl.  Families: XFA_IMPL_AUTO,
+ * XFA_IMPL_TCGEN05 (bf16, hd 64 / 128) and XFA_IMPL_SIMT; the backward with
+ * XFA_IMPL_TCGEN05_DET and p_drop > 0 returns XFA_ERR_UNSUPPORTED.
+ */
+int xfa_fwd_dropout(const void *q, const void *k, const void *v, void *out, float *lse,
+                    int bh, int S, int hd, float scale, int dtype,
+                    float p_drop, unsigned long long seed, int impl, void *stream);
+
+int xfa_bwd_dropout(const void *q, const void *k, const void *v, const void *out, const void *dout,
+                    const float *lse, void *dq, void *dk, void *dv,
+                    int bh, int S, int hd, float scale, int dtype,
+                    float p_drop, unsigned long long seed,
+                    void *workspace, size_t workspace_bytes, int impl, void *stream);
+
+/*
  * The three stages of xfa_bwd as separate calls, for callers that schedule
  * (or time) them individually.  xfa_bwd_impl is exactly prep, main, finish
  * in this order on one stream, with the same arguments and workspace.

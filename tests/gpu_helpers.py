@@ -26,13 +26,15 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def run_gpu(x, dtype: str, scale: float, impl: int = 0, backward: bool = True):
+def run_gpu(x, dtype: str, scale: float, impl: int = 0, backward: bool = True, dropout=None):
+    """``dropout = (p, seed)``: dropout on the attention probabilities."""
     from bwd_xfa_fwd_gb300 import binding
+    p_drop, seed = (0.0, 0) if dropout is None else dropout
     q, k, v, do = (to_device(x[n], dtype) for n in ("q", "k", "v", "dout"))
-    out, lse = binding.fwd(q, k, v, scale, impl)
+    out, lse = binding.fwd(q, k, v, scale, impl, dropout_p=p_drop, seed=seed)
     res = {"out": out, "lse": lse}
     if backward:
-        dq, dk, dv = binding.bwd(q, k, v, out, do, lse, scale, impl)
+        dq, dk, dv = binding.bwd(q, k, v, out, do, lse, scale, impl, dropout_p=p_drop, seed=seed)
         res.update(dq=dq, dk=dk, dv=dv)
     torch.cuda.synchronize()
     assert binding.status() == binding.XFA_OK
@@ -71,10 +73,10 @@ def compare(got: dict, ref: dict, dtype: str, heads=None, names=("out", "lse", "
 _ORACLE_CACHE = {}
 
 
-def oracle_result(key, x, scale, heads=None):
-    """Oracle on inputs ``x`` (fp64 views), memoised under ``key``."""
-    k = (key, None if heads is None else tuple(heads))
+def oracle_result(key, x, scale, heads=None, dropout=None):
+    """Oracle on inputs ``x`` (fp64 views), memoised under ``key``; ``dropout = (p, seed)``."""
+    k = (key, None if heads is None else tuple(heads), dropout)
     if k not in _ORACLE_CACHE:
         _ORACLE_CACHE[k] = oracle.attention(x["q"].exact, x["k"].exact, x["v"].exact, x["dout"].exact, scale,
-                                            heads=heads)
+                                            heads=heads, dropout=dropout)
     return _ORACLE_CACHE[k]

@@ -190,7 +190,7 @@ def pin_dropout_generator_outputs(orc):
 def pin_dropout_keep_known_answers(orc):
     """keep() against the page's definition worked by hand from the published outputs:
     (seed, index) = (0, 0) gives key 0 and h = 0xE220A8397B1DCDAF, so u = 0xE220A8 / 2^24
-    = 0.883300...; (0, 1) gives key = gamma, h = 0x6E789E6AA1B965F4, u = 0.431528...;
+    = 0.883311...; (0, 1) gives key = gamma, h = 0x6E789E6AA1B965F4, u = 0.431528...;
     (2 gamma, 0) gives key = 2 gamma, h = 0x06C45D188009454F, u = 0.026433...
     Each element is kept for p just below its u and dropped for p just above."""
     for seed, index, u in ((0, 0, 0.8833), (0, 1, 0.43153), ((2 * GOLDEN_GAMMA) % 2 ** 64, 0, 0.026433)):

@@ -1,0 +1,149 @@
+"""Dropout on the attention probabilities (xfa_fwd_dropout / xfa_bwd_dropout) against
+the CPU oracle (GB300 only).  The mask itself is checked bit for bit: with S = hd and
+V = I the forward's output is P o C, with dO = I the backward's dV is (P o C)^T, so an
+element is nonzero exactly when the oracle's keep() keeps it.  Every call goes through
+the C ABI (ctypes binding)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bwd_xfa_fwd_gb300 import inputs
+from tests.gpu_helpers import compare, oracle_result, run_gpu, to_device, to_f64
+
+pytestmark = pytest.mark.gpu
+
+FAMILIES = [("bf16", 128, 2), ("bf16", 64, 2), ("bf16", 64, 1), ("f32", 32, 1), ("f32", 64, 1), ("f32", 128, 1)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from bwd_xfa_fwd_gb300 import binding, build
+    build.build()
+    binding.load()
+    assert torch.cuda.is_available()
+
+
+@pytest.mark.parametrize("p", [0.1, 0.5])
+@pytest.mark.parametrize("S", [300, 777])
+@pytest.mark.parametrize("dtype,hd,impl", FAMILIES)
+def test_dropout_against_oracle(dtype, hd, impl, S, p):
+    bh = 2
+    scale = 1.0 / math.sqrt(hd)
+    x = inputs.draw((bh, S, hd), dtype, seed=500 + S + hd)
+    seed = 0x5EED0000 + S
+    got = run_gpu(x, dtype, scale, impl=impl, dropout=(p, seed))
+    ref = oracle_result(("drop", S, hd, dtype), x, scale, dropout=(p, seed))
+    compare(got, ref, dtype)
+
+
+def _kept_reference(bh, S, p, seed):
+    """keep(seed, (b*S + i)*S + j, p) of the pinned oracle, for j <= i (above the
+    diagonal the probabilities are 0 whatever the mask)."""
+    k = np.zeros((bh, S, S), dtype=bool)
+    for b in range(bh):
+        for i in range(S):
+            base = (b * S + i) * S
+            for j in range(i + 1):
+                k[b, i, j] = oracle.keep(seed, base + j, p)
+    return k
+
+
+@pytest.mark.parametrize("dtype,hd,impl", FAMILIES)
+def test_dropout_mask_bit_for_bit(dtype, hd, impl):
+    from bwd_xfa_fwd_gb300 import binding
+    bh, S, p, seed = 2, hd, 0.3, 0xA5A5A5A5DEADBEEF
+    x = inputs.draw((bh, S, hd), dtype, seed=7, stds=(0.3, 0.3, 1.0, 1.0))
+    eye = np.broadcast_to(np.eye(S, dtype=np.float32), (bh, S, S)).copy()
+    ident = inputs._stored(eye, dtype)
+    q, k = to_device(x["q"], dtype), to_device(x["k"], dtype)
+    v = to_device(ident, dtype)
+    do = to_device(ident, dtype)
+    scale = 1.0 / math.sqrt(hd)
+    out, lse = binding.fwd(q, k, v, scale, impl, dropout_p=p, seed=seed)
+    dq, dk, dv = binding.bwd(q, k, v, out, do, lse, scale, impl, dropout_p=p, seed=seed)
+    torch.cuda.synchronize()
+    assert binding.status() == binding.XFA_OK
+    want = _kept_reference(bh, S, p, seed)
+    lower = np.tril(np.ones((S, S), dtype=bool))
+    got_fwd = to_f64(out) != 0.0                      # O = P o C   (V = I)
+    got_bwd = np.swapaxes(to_f64(dv), 1, 2) != 0.0    # dV^T = P o C   (dO = I)
+    for name, got in (("forward", got_fwd), ("backward", got_bwd)):
+        bad = (got != want) & lower
+        assert not bad.any(), f"{name}: {int(bad.sum())} mask bits differ, first at {np.argwhere(bad)[0].tolist()}"
+    kept = want[:, lower].mean()
+    assert abs(kept - (1 - p)) < 0.05, kept
+
+
+@pytest.mark.parametrize("dtype,hd,impl", [("bf16", 128, 2), ("f32", 64, 1)])
+def test_rate_zero_is_the_plain_operator(dtype, hd, impl):
+    from bwd_xfa_fwd_gb300 import binding
+    x = inputs.draw((2, 200, hd), dtype, seed=11)
+    q, k, v, do = (to_device(x[n], dtype) for n in ("q", "k", "v", "dout"))
+    lib = binding.load()
+    outs = []
+    for use_dropout_entry in (False, True):
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:-1], device="cuda", dtype=torch.float32)
+        st = binding._stream(q)
+        args = (binding._p(q), binding._p(k), binding._p(v), binding._p(out), binding._p(lse), 2, 200, hd, 0.1,
+                binding._DTYPE[q.dtype])
+        if use_dropout_entry:
+            rc = lib.xfa_fwd_dropout(*args, 0.0, 99, impl, st)
+        else:
+            rc = lib.xfa_fwd_impl(*args, impl, st)
+        assert rc == binding.XFA_OK
+        grads = binding.bwd(q, k, v, out, do, lse, 0.1, impl, dropout_p=0.0, seed=99)
+        torch.cuda.synchronize()
+        outs.append([out, lse, *grads])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
+def test_same_seed_same_result_other_seed_other_mask():
+    x = inputs.draw((1, 256, 64), "bf16", seed=12)
+    a = run_gpu(x, "bf16", 0.125, dropout=(0.2, 1))
+    b = run_gpu(x, "bf16", 0.125, dropout=(0.2, 1))
+    c = run_gpu(x, "bf16", 0.125, dropout=(0.2, 2))
+    for n in a:
+        assert np.array_equal(a[n], b[n]), n
+    assert not np.array_equal(a["out"], c["out"])
+    assert np.array_equal(a["lse"], c["lse"])   # the softmax itself is not dropped
+
+
+def test_full_size_sampled_head_with_dropout():
+    w = inputs.WORKLOADS[5]
+    x = inputs.workload_inputs(w)
+    got = run_gpu(x, w.dtype, w.scale, dropout=(0.1, 2024))
+    ref = oracle_result(("w5drop",), x, w.scale, heads=[31], dropout=(0.1, 2024))
+    compare(got, ref, w.dtype, heads=[31])
+
+
+def test_dropout_rejections():
+    from bwd_xfa_fwd_gb300 import binding
+    x = inputs.draw((1, 128, 64), "bf16", seed=3)
+    q, k, v, do = (to_device(x[n], "bf16") for n in ("q", "k", "v", "dout"))
+    for bad in (1.0, -0.1, float("nan"), 1.5):
+        with pytest.raises(binding.XfaError) as e:
+            binding.fwd(q, k, v, 0.1, dropout_p=bad, seed=1)
+        assert e.value.code == binding.XFA_ERR_INVALID_ARG
+    out, lse = binding.fwd(q, k, v, 0.1, dropout_p=0.2, seed=1)
+    with pytest.raises(binding.XfaError) as e:
+        binding.bwd(q, k, v, out, do, lse, 0.1, binding.IMPL_TCGEN05_DET, dropout_p=0.2, seed=1)
+    assert e.value.code == binding.XFA_ERR_UNSUPPORTED
+
+
+def test_tape_node_with_dropout():
+    from bwd_xfa_fwd_gb300 import binding, tape
+    x = inputs.draw((2, 300, 128), "bf16", seed=21)
+    dev = {n: to_device(x[n], "bf16") for n in ("q", "k", "v", "dout")}
+    qv, kv, vv = (tape.Var(dev[n]) for n in ("q", "k", "v"))
+    o = tape.flash_attention(qv, kv, vv, dropout_p=0.25, seed=77)
+    o.backward(seed=dev["dout"])
+    torch.cuda.synchronize()
+    ref = run_gpu(x, "bf16", binding.default_scale(128), dropout=(0.25, 77))
+    assert np.array_equal(to_f64(o.value), ref["out"])
+    for var, n in ((qv, "dq"), (kv, "dk"), (vv, "dv")):
+        assert np.array_equal(to_f64(var.grad), ref[n]), n
