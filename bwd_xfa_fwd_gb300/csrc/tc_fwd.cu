@@ -107,6 +107,22 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
         mma_ts(o_tmem, p_tmem + ks * 8, sdesc_advance(v_desc, ks * 2048), idesc, (accumulate || ks > 0) ? 1u : 0u);
 }
 
+// Raw scores of columns 64h..64h+63 of this thread's row of S_t (TMEM lane); on the
+// diagonal key tile the keys past the row (column > r) become -inf.
+__device__ __forceinline__ void load_scores_half(uint32_t tS, int h, bool diag, int r, uint32_t *sh)
+{
+    tmem_ld32(tS + 64 * h, sh);
+    tmem_ld32(tS + 64 * h + 32, sh + 32);
+    tmem_wait_ld();
+    reg_fence32(sh);
+    reg_fence32(sh + 32);
+    if (diag) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+            if (64 * h + c > r) sh[c] = 0xff800000u;   // -inf
+    }
+}
+
 // DROP: dropout on the probabilities that enter P.V (the row sums l keep every p).
 template <int HD, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -279,35 +295,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < n_mine; ++j) {
             if (!(ok = warp_wait(&bars->s_full[t], j & 1, bars, status))) break;
             tc_fence_after_sync();
-            uint32_t sr[128];
-            tmem_ld32(tS + 0, sr + 0);
-            tmem_ld32(tS + 32, sr + 32);
-            tmem_ld32(tS + 64, sr + 64);
-            tmem_ld32(tS + 96, sr + 96);
-            tmem_wait_ld();
-            reg_fence32(sr + 0);
-            reg_fence32(sr + 32);
-            reg_fence32(sr + 64);
-            reg_fence32(sr + 96);
-            // raw scores; the diagonal tile masks keys past the row
-            if (j == diag) {
+            // pass 1: row maximum, the scores read from TMEM in two 64-column halves (so only half
+            // a row is held in registers); the diagonal tile masks keys past the row.  4 independent
+            // chains of 3-input maxima.
+            const bool on_diag = j == diag;
+            float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (c > r) sr[c] = 0xff800000u;   // -inf
+            for (int h = 0; h < 2; ++h) {
+                uint32_t sh[64];
+                load_scores_half(tS, h, on_diag, r, sh);
+#pragma unroll
+                for (int c = 0; c < 64; c += 8)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        mx4[e] = fmax3(mx4[e], __uint_as_float(sh[c + 2 * e]), __uint_as_float(sh[c + 2 * e + 1]));
             }
-            // row max: 4 independent chains of 3-input maxima over columns 0..127
-            // (chain e starts at column e, then takes two columns per step from 4 + 8k + 2e;
-            // the last four columns 124..127 are folded in singly)
-            float mx4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) mx4[e] = __uint_as_float(sr[e]);
-#pragma unroll
-            for (int c = 4; c + 8 <= 124; c += 8)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    mx4[e] = fmax3(mx4[e], __uint_as_float(sr[c + 2 * e]), __uint_as_float(sr[c + 2 * e + 1]));
-#pragma unroll
-            for (int e = 0; e < 4; ++e) mx4[e] = fmaxf(mx4[e], __uint_as_float(sr[124 + e]));
             const float mx = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
             const float m_new = fmaxf(m, mx * scale_log2);   // scale > 0: max commutes with the scaling
             const bool need = m_new > m + kRescaleThreshold;
@@ -333,13 +335,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t c2 = f2_pack(scale_log2, scale_log2);
             const uint64_t nm2 = f2_pack(-m, -m);
             uint64_t l2[4] = {0ull, 0ull, 0ull, 0ull};
+            // pass 2: the exponentials, half a row at a time (the scores read again)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
+                uint32_t sh[64];
+                load_scores_half(tS, h, on_diag, r, sh);
                 uint32_t pk[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int c = 64 * h + 2 * e;
-                    const float2 a = f2_unpack(ffma2(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, nm2));
+                    const float2 a = f2_unpack(ffma2(f2_pack(__uint_as_float(sh[2 * e]), __uint_as_float(sh[2 * e + 1])), c2, nm2));
                     const float p0 = ex2_approx(a.x);
                     const float p1 = ex2_approx(a.y);
                     l2[e & 3] = fadd2(l2[e & 3], f2_pack(p0, p1));
