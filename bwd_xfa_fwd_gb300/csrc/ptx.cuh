@@ -145,9 +145,6 @@ __device__ __forceinline__ void bulk_wait_group_read0()
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
-// Wait until every bulk group of this thread has completed.
-__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
 {
@@ -303,15 +300,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r)
         : "r"(taddr));
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r)
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : XFA_R8(0), XFA_R8(8)
-        : "r"(taddr));
-}
-
 __device__ __forceinline__ void tmem_wait_ld()
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -322,11 +310,6 @@ __device__ __forceinline__ void tmem_wait_ld()
 __device__ __forceinline__ void reg_fence32(uint32_t *r)
 {
     asm volatile("" : XFA_F8(0), XFA_F8(8), XFA_F8(16), XFA_F8(24));
-}
-
-__device__ __forceinline__ void reg_fence16(uint32_t *r)
-{
-    asm volatile("" : XFA_F8(0), XFA_F8(8));
 }
 
 // Store 32 / 16 consecutive 32-bit columns of this warp's 32 TMEM lanes.
