@@ -18,7 +18,6 @@ import argparse
 import csv
 import io
 import json
-import math
 import os
 import subprocess
 import sys

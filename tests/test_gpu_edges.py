@@ -5,7 +5,6 @@ the C ABI (ctypes binding)."""
 import ctypes
 import math
 
-import numpy as np
 import pytest
 import torch
 

@@ -15,7 +15,7 @@ import pytest
 import torch
 
 from bwd_xfa_fwd_gb300 import inputs
-from tests.gpu_helpers import TOL, compare, to_device, to_f64
+from tests.gpu_helpers import compare, to_device, to_f64
 
 pytestmark = pytest.mark.gpu
 
