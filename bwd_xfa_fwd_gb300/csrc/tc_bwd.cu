@@ -29,6 +29,9 @@
 //                         dQ^T [2hd+128,2hd+192) K_j [2hd+192,2hd+192+hd/2).
 // For hd = 64 the dQ^T MMA still runs with M = 128; lanes 64-127 hold
 // products of V and are never read.
+// Without the fused dQ (the deterministic variant) the dQ^T columns hold a second
+// S^T buffer: tiles alternate between the two, and S^T of the next tile is issued
+// before this tile's dV, so the key warps do not wait for it.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -69,6 +72,12 @@ struct Cfg {
     // dP^T (dS^T bf16 written back into its first 32 columns); dQ^T; K_j as a bf16 A operand.
     static constexpr uint32_t COL_DK = 0, COL_DV = HD, COL_S = 2 * HD, COL_DP = 2 * HD + 64,
                               COL_DQ = 2 * HD + 128, COL_KT = 2 * HD + 192;
+    // S^T buffer of query tile i: with the fused dQ one buffer; without it (the dQ^T
+    // columns are free) tiles alternate between COL_S and COL_DQ.
+    static __device__ __forceinline__ uint32_t col_s(bool two_buffers, int i)
+    {
+        return two_buffers && (i & 1) ? COL_DQ : COL_S;
+    }
     static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -77,7 +86,7 @@ constexpr int kMaxRing = 4;
 struct Bars {
     uint64_t kv_full;
     uint64_t q_full[kMaxRing], q_empty[kMaxRing];
-    uint64_t s_full, p_full, ds_full[2], ds_empty[2];
+    uint64_t s_full[2], p_full, ds_full[2], ds_empty[2];
     uint64_t kt_full, dp_full, dq_full, dq_empty, done, drain;
     uint32_t tmem_base;
     int abort;
@@ -205,7 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->ds_full[b], 4);   // one arrival per key warp
             mbar_init(&bars->ds_empty[b], 1);
         }
-        mbar_init(&bars->s_full, 1);
+        mbar_init(&bars->s_full[0], 1);
+        mbar_init(&bars->s_full[1], 1);
         mbar_init(&bars->p_full, 4);
         mbar_init(&bars->kt_full, 4);
         mbar_init(&bars->dp_full, 1);
@@ -283,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             if (leader) {
                 issue_s<HD>(tmem + C::COL_S, tmem + C::COL_KT, q_km, idesc_s);
-                tc_commit(&bars->s_full);
+                tc_commit(&bars->s_full[0]);
                 issue_rows_dot<HD>(tmem + C::COL_DP, v_km, do_km);
                 tc_commit(&bars->dp_full);
             }
@@ -294,22 +304,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ph2 = (it >> 1) & 1;
             const uint32_t qoff = st * C::Q_BYTES, dsoff = b * C::DS_BYTES;
             const int nx = it + 1, stn = nx % NSQ;
-            // dV += P^T dO_i  (P^T: bf16 in the first columns of S^T)
+            // Next S^T.  Without the fused dQ it goes first, into the other S^T buffer, so that it
+            // does not queue behind this tile's work (that buffer's P^T, tile it - 1, was read by
+            // the dV MMA issued one iteration ago, and the in-order pipe runs that MMA first).
+            // With one buffer it follows this tile's dV, which reads P^T from the same columns.
+            const bool s_first = !FUSED_DQ && nx < n;
+            if (s_first) {
+                if (!(ok = warp_wait(&bars->q_full[stn], (nx / NSQ) & 1, bars, status))) break;
+                tc_fence_after_sync();
+                if (leader) {
+                    issue_s<HD>(tmem + C::col_s(true, nx), tmem + C::COL_KT, sdesc_advance(q_km, stn * C::Q_BYTES),
+                                idesc_s);
+                    tc_commit(&bars->s_full[nx & 1]);
+                }
+                __syncwarp();
+            }
+            // dV += P^T dO_i  (P^T: bf16 in the first columns of this tile's S^T)
             if (!(ok = warp_wait(&bars->p_full, it & 1, bars, status))) break;
             tc_fence_after_sync();
             if (leader) {
 #pragma unroll
                 for (int ks = 0; ks < BM / 16; ++ks)
-                    mma_ts(tmem + C::COL_DV, tmem + C::COL_S + ks * 8, sdesc_advance(do_mn, qoff + ks * 2048), idesc_acc,
-                           (it > 0 || ks > 0) ? 1u : 0u);
+                    mma_ts(tmem + C::COL_DV, tmem + C::col_s(!FUSED_DQ, it) + ks * 8,
+                           sdesc_advance(do_mn, qoff + ks * 2048), idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
             }
             __syncwarp();
-            if (nx < n) {   // next S^T: its columns are free once the dV MMA above has read P^T (in order)
+            if (FUSED_DQ && nx < n) {   // next S^T: its columns are free once the dV MMA above has read P^T
                 if (!(ok = warp_wait(&bars->q_full[stn], (nx / NSQ) & 1, bars, status))) break;
                 tc_fence_after_sync();
                 if (leader) {
                     issue_s<HD>(tmem + C::COL_S, tmem + C::COL_KT, sdesc_advance(q_km, stn * C::Q_BYTES), idesc_s);
-                    tc_commit(&bars->s_full);
+                    tc_commit(&bars->s_full[0]);
                 }
                 __syncwarp();
             }
@@ -382,11 +407,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int i0 = (it0 + it) * BM;
             const float *Ls = ld_s + st * 2 * BM;
             const float *Ds = Ls + BM;
-            if (!(ok = warp_wait(&bars->s_full, it & 1, bars, status))) break;
+            // S^T of this tile: one buffer (phase per tile) or two alternating (phase per pair)
+            const uint32_t t_s = tmem + lane_off + C::col_s(!FUSED_DQ, it);
+            if (!(ok = FUSED_DQ ? warp_wait(&bars->s_full[0], it & 1, bars, status)
+                                : warp_wait(&bars->s_full[b], ph2, bars, status)))
+                break;
             tc_fence_after_sync();
             uint32_t sr[64];
-            tmem_ld32(tmem + lane_off + C::COL_S, sr);
-            tmem_ld32(tmem + lane_off + C::COL_S + 32, sr + 32);
+            tmem_ld32(t_s, sr);
+            tmem_ld32(t_s + 32, sr + 32);
             tmem_wait_ld();
             reg_fence32(sr);
             reg_fence32(sr + 32);
@@ -427,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                tmem_st32(tmem + lane_off + C::COL_S, pk);
+                tmem_st32(t_s, pk);
                 tmem_wait_st();
             }
             tc_fence_before_sync();
