@@ -5,6 +5,7 @@ in full; workloads 4-5 (S=4096 and S=8192) in the launch configuration the
 benchmark times, on sampled heads the oracle computes exactly, plus identities
 that hold for every head at any size."""
 import math
+import os
 
 import numpy as np
 import pytest
@@ -236,8 +237,11 @@ def test_tape_node_with_deterministic_backward():
     compare(got, oracle_result(("tape-det",), x, scale), "bf16", names=("out", "dq", "dk", "dv"))
 
 
-def _fuzz_cases(n=24, seed=2024):
+def _fuzz_cases(n=int(os.environ.get("XFA_FUZZ_CASES", "24")), seed=2024):
+    """Seeded random cases; XFA_FUZZ_CASES raises their number for a longer soak.  The
+    dropout rate comes from a second generator so the other draws stay as they were."""
     rng = np.random.default_rng(seed)
+    rng_drop = np.random.default_rng(seed + 1)
     cases = []
     for i in range(n):
         dtype = "bf16" if i % 4 else "f32"
@@ -247,14 +251,17 @@ def _fuzz_cases(n=24, seed=2024):
         bh = int(rng.integers(1, 5))
         scale = float(rng.uniform(0.02, 0.3))
         std = float(rng.choice([0.5, 1.0, 2.0, 3.0]))
-        cases.append((i, dtype, hd, impl, S, bh, scale, std))
+        p_drop = float(rng_drop.choice([0.0, 0.0, 0.1, 0.3])) if impl != 3 else 0.0
+        cases.append((i, dtype, hd, impl, S, bh, scale, std, p_drop))
     return cases
 
 
-@pytest.mark.parametrize("case", _fuzz_cases(), ids=lambda c: f"{c[0]}-{c[1]}-hd{c[2]}-impl{c[3]}-S{c[4]}-bh{c[5]}")
+@pytest.mark.parametrize("case", _fuzz_cases(),
+                         ids=lambda c: f"{c[0]}-{c[1]}-hd{c[2]}-impl{c[3]}-S{c[4]}-bh{c[5]}-p{c[8]}")
 def test_random_shapes_against_oracle(case):
-    """Seeded random shapes, scales, input spreads and kernel families."""
-    i, dtype, hd, impl, S, bh, scale, std = case
+    """Seeded random shapes, scales, input spreads, kernel families and dropout rates."""
+    i, dtype, hd, impl, S, bh, scale, std, p_drop = case
     x = inputs.draw((bh, S, hd), dtype, seed=7000 + i, stds=(std, std, 1.0, 1.0))
-    got = run_gpu(x, dtype, scale, impl=impl)
-    compare(got, oracle_result(("fuzz", i), x, scale), dtype)
+    drop = (p_drop, 9000 + i) if p_drop else None
+    got = run_gpu(x, dtype, scale, impl=impl, dropout=drop)
+    compare(got, oracle_result(("fuzz", i), x, scale, dropout=drop), dtype)
