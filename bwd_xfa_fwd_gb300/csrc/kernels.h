@@ -75,6 +75,11 @@ int launch_tc_bwd(const BwdParams &p, cudaStream_t st, bool fused_dq);
 // Query-tile dQ pass: writes p.dq (bf16) directly, no atomics.
 int launch_tc_dq(const BwdParams &p, cudaStream_t st);
 
+// 3xTF32 tensor-core family: fp32, hd in {32, 64}.  Return an XFA_* code.
+int launch_tf_fwd(const FwdParams &p, cudaStream_t st);
+// dK, dV by key tiles, then dQ by query tiles (no atomics); writes p.dq / p.dk / p.dv.
+int launch_tf_bwd(const BwdParams &p, cudaStream_t st);
+
 // Encodes the TMA descriptors; resolved once from the driver (xfa_api.cu).
 int encode_tmap_bf16_3d(void *tmap, const void *base, int hd, int S, int bh, int box_rows);
 

@@ -82,7 +82,10 @@ int validate_shape(int bh, int S, int hd, float scale, int dtype)
 
 bool tc_supported(int hd, int dtype) { return dtype == XFA_BF16 && (hd == 64 || hd == 128); }
 
-enum class Family { Simt, TcFused, TcDet };
+// fp32 on the tensor cores (3xTF32): hd 32 and 64 (hd 128 fp32 tiles do not fit shared memory).
+bool tf_supported(int hd, int dtype) { return dtype == XFA_F32 && (hd == 32 || hd == 64); }
+
+enum class Family { Simt, TcFused, TcDet, Tf32 };
 
 // The tcgen05 backward variant XFA_IMPL_AUTO resolves to.
 constexpr Family kAutoTc = Family::TcFused;
@@ -94,12 +97,20 @@ int choose_impl(int impl, int hd, int dtype, Family *fam)
     case XFA_IMPL_SIMT: *fam = Family::Simt; return XFA_OK;
     case XFA_IMPL_TCGEN05:
     case XFA_IMPL_TCGEN05_DET:
+        if (tf_supported(hd, dtype)) {
+            if (!device_is_sm103()) return XFA_ERR_DEVICE;
+            *fam = Family::Tf32;   // one kernel family for fp32, deterministic by construction
+            return XFA_OK;
+        }
         if (!tc_supported(hd, dtype)) return XFA_ERR_UNSUPPORTED;
         if (!device_is_sm103()) return XFA_ERR_DEVICE;
         *fam = impl == XFA_IMPL_TCGEN05 ? Family::TcFused : Family::TcDet;
         return XFA_OK;
     case XFA_IMPL_AUTO:
-        *fam = (tc_supported(hd, dtype) && device_is_sm103()) ? kAutoTc : Family::Simt;
+        if (!device_is_sm103()) *fam = Family::Simt;
+        else if (tc_supported(hd, dtype)) *fam = kAutoTc;
+        else if (tf_supported(hd, dtype)) *fam = Family::Tf32;
+        else *fam = Family::Simt;
         return XFA_OK;
     default: return XFA_ERR_INVALID_ARG;
     }
@@ -203,10 +214,12 @@ static int fwd_run(const void *q, const void *k, const void *v, void *out, float
         return XFA_ERR_INVALID_ARG;
     Family fam;
     if ((rc = choose_impl(impl, hd, dtype, &fam)) != XFA_OK) return rc;
+    if (drop.on && fam == Family::Tf32 && impl == XFA_IMPL_AUTO) fam = Family::Simt;   // no fp32 tensor-core dropout
     FwdParams p{q, k, v, out, lse, bh, S, hd, scale, dtype, nullptr};
     p.drop = drop;
     if ((rc = status_ptr(&p.status)) != XFA_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (fam == Family::Tf32) return launch_tf_fwd(p, st);
     if (fam != Family::Simt) return launch_tc_fwd(p, st);
     return cuda_code(launch_simt_fwd(p, st));
 }
@@ -270,7 +283,7 @@ static const void *unused_ptr(const void *p) { return p; }
 // The three stages of one backward for the resolved family.
 static int stage_prep(BwdParams p, Family fam, cudaStream_t st)
 {
-    if (fam == Family::TcDet) p.dq_acc = nullptr;   // no accumulator to clear
+    if (fam == Family::TcDet || fam == Family::Tf32) p.dq_acc = nullptr;   // no accumulator to clear
     return cuda_code(launch_bwd_prep(p, st));
 }
 
@@ -283,6 +296,7 @@ static int stage_main(const BwdParams &p, Family fam, cudaStream_t st)
         int rc = launch_tc_bwd(p, st, false);
         return rc == XFA_OK ? launch_tc_dq(p, st) : rc;
     }
+    case Family::Tf32: return launch_tf_bwd(p, st);
     }
     return XFA_ERR_INVALID_ARG;
 }
@@ -343,6 +357,7 @@ static int bwd_run(const void *q, const void *k, const void *v, const void *out,
     p.drop = drop;
     Family fam;
     if ((rc = choose_impl(impl, hd, dtype, &fam)) != XFA_OK) return rc;
+    if (drop.on && fam == Family::Tf32 && impl == XFA_IMPL_AUTO) fam = Family::Simt;   // as in fwd_run
     if (drop.on && fam == Family::TcDet) return XFA_ERR_UNSUPPORTED;   // dropout: fused and SIMT families only
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if ((rc = stage_prep(p, fam, st)) != XFA_OK) return rc;

@@ -25,11 +25,12 @@ def built():
     assert torch.cuda.is_available()
 
 
+@pytest.mark.parametrize("impl", [0, 1], ids=["auto", "simt"])
 @pytest.mark.parametrize("wid", [1, 2, 3])
-def test_workload_full(wid):
+def test_workload_full(wid, impl):
     w = inputs.WORKLOADS[wid]
     x = inputs.workload_inputs(w)
-    got = run_gpu(x, w.dtype, w.scale)
+    got = run_gpu(x, w.dtype, w.scale, impl=impl)
     ref = oracle_result(("w", wid), x, w.scale)
     compare(got, ref, w.dtype)
 
@@ -69,7 +70,7 @@ RAGGED = [1, 5, 64, 100, 128, 129, 255, 256, 257, 300, 511, 777]
 @pytest.mark.parametrize("S", RAGGED)
 @pytest.mark.parametrize("dtype,hd,impl", [("bf16", 128, 2), ("bf16", 64, 2), ("bf16", 128, 3), ("bf16", 64, 3),
                                            ("bf16", 32, 1), ("f32", 32, 1), ("f32", 64, 1), ("f32", 128, 1),
-                                           ("bf16", 128, 1)])
+                                           ("bf16", 128, 1), ("f32", 32, 2), ("f32", 64, 2)])
 def test_ragged_and_small(S, dtype, hd, impl):
     bh = 3
     scale = 1.0 / math.sqrt(hd)
