@@ -19,6 +19,7 @@
 // operand is K-major.
 #include <math_constants.h>
 
+#include "dropout.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tf32x3.cuh"
@@ -159,12 +160,13 @@ struct KvCfg {
     static_assert(DK + HD <= 512, "TMEM columns");
 };
 
-template <int HD>
+// DROP: dropout's backward (dV takes P o C, dS takes C o dP; see dropout.cuh for C).
+template <int HD, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     tf_bwd_kv_kernel(const float *__restrict__ Q, const float *__restrict__ K, const float *__restrict__ V,
                      const float *__restrict__ dO, const float *__restrict__ Dg, const float *__restrict__ Lg,
                      float *__restrict__ dK, float *__restrict__ dV, int bh, int S, int S_pad, float scale,
-                     float scale_log2, int *status)
+                     float scale_log2, int *status, const DropParams drop)
 {
     using C = KvCfg<HD>;
     extern __shared__ uint8_t smem_raw[];
@@ -297,8 +299,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 4; ++e) {
                     const int c = 4 * c4 + e;
                     const float p = key <= q0 + c ? ex2_approx(fmaf(__uint_as_float(s[c]), scale_log2, lgs[e])) : 0.0f;
-                    const float ds = p * (__uint_as_float(dp[c]) - dds[e]) * scale;
-                    split_tf32(p, p_hi[c], p_lo[c]);
+                    float dpc = __uint_as_float(dp[c]), pv = p;
+                    if (DROP) {
+                        // element (q0 + c, key): flat index (head*S + q0 + c)*S + key
+                        const uint64_t g =
+                            (((uint64_t)head * S + (uint64_t)(q0 + c)) * (uint64_t)S + (uint64_t)key) * kDropGolden;
+                        const bool keep = drop_keep(drop.seed, g, drop.keep_thr);
+                        pv = keep ? p * drop.inv_keep : 0.0f;
+                        dpc = keep ? dpc * drop.inv_keep : 0.0f;
+                    }
+                    const float ds = p * (dpc - dds[e]) * scale;
+                    split_tf32(pv, p_hi[c], p_lo[c]);
                     split_tf32(ds, s[c], dp[c]);   // s, dp now hold dS^T hi / lo
                 }
             }
@@ -343,11 +354,12 @@ struct QCfg {
     static_assert(DQ + HD <= 512, "TMEM columns");
 };
 
-template <int HD>
+template <int HD, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     tf_bwd_q_kernel(const float *__restrict__ Q, const float *__restrict__ K, const float *__restrict__ V,
                     const float *__restrict__ dO, const float *__restrict__ Dg, const float *__restrict__ Lg,
-                    float *__restrict__ dQ, int bh, int S, int S_pad, float scale, float scale_log2, int *status)
+                    float *__restrict__ dQ, int bh, int S, int S_pad, float scale, float scale_log2, int *status,
+                    const DropParams drop)
 {
     using C = QCfg<HD>;
     extern __shared__ uint8_t smem_raw[];
@@ -463,10 +475,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             reg_fence32(s);
             reg_fence32(dp);
             const int kmax = row - j * BS;   // columns past this are keys after the row
+            // dropout: element (row, key) has flat index (head*S + row)*S + key
+            uint64_t drop_g =
+                DROP ? (((uint64_t)head * S + (uint64_t)row) * (uint64_t)S + (uint64_t)(j * BS)) * kDropGolden : 0ull;
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
                 const float p = c <= kmax ? ex2_approx(fmaf(__uint_as_float(s[c]), scale_log2, lg)) : 0.0f;
-                split_tf32(p * (__uint_as_float(dp[c]) - dd) * scale, s[c], dp[c]);   // dS hi / lo
+                float dpc = __uint_as_float(dp[c]);
+                if (DROP) {
+                    dpc = drop_keep(drop.seed, drop_g, drop.keep_thr) ? dpc * drop.inv_keep : 0.0f;
+                    drop_g += kDropGolden;
+                }
+                split_tf32(p * (dpc - dd) * scale, s[c], dp[c]);   // dS hi / lo
             }
             tmem_st32(t + C::DP, s);
             tmem_st32(t + C::DSLO, dp);
@@ -496,24 +516,24 @@ int set_smem(Kern kern, int bytes)
     return e == cudaSuccess ? XFA_OK : XFA_ERR_CUDA_BASE + (int)e;
 }
 
-template <int HD>
+template <int HD, bool DROP>
 int run(const BwdParams &p, cudaStream_t st)
 {
     static_assert(KvCfg<HD>::SMEM <= 227 * 1024 && QCfg<HD>::SMEM <= 227 * 1024, "shared memory per CTA");
     const float scale_log2 = p.scale * 1.4426950408889634f;
     const unsigned grid = (unsigned)(((p.S + BT - 1) / BT) * p.bh);
-    auto kv = tf_bwd_kv_kernel<HD>;
-    auto qk = tf_bwd_q_kernel<HD>;
+    auto kv = tf_bwd_kv_kernel<HD, DROP>;
+    auto qk = tf_bwd_q_kernel<HD, DROP>;
     int rc = set_smem(kv, KvCfg<HD>::SMEM);
     if (rc == XFA_OK) rc = set_smem(qk, QCfg<HD>::SMEM);
     if (rc != XFA_OK) return rc;
     const float *q = (const float *)p.q, *k = (const float *)p.k, *v = (const float *)p.v, *dout = (const float *)p.dout;
     kv<<<grid, kThreads, KvCfg<HD>::SMEM, st>>>(q, k, v, dout, p.D, p.Lg, (float *)p.dk, (float *)p.dv, p.bh, p.S,
-                                                 p.S_pad, p.scale, scale_log2, p.status);
+                                                 p.S_pad, p.scale, scale_log2, p.status, p.drop);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return XFA_ERR_CUDA_BASE + (int)e;
     qk<<<grid, kThreads, QCfg<HD>::SMEM, st>>>(q, k, v, dout, p.D, p.Lg, (float *)p.dq, p.bh, p.S, p.S_pad, p.scale,
-                                                scale_log2, p.status);
+                                                scale_log2, p.status, p.drop);
     e = cudaGetLastError();
     return e == cudaSuccess ? XFA_OK : XFA_ERR_CUDA_BASE + (int)e;
 }
@@ -522,9 +542,9 @@ int run(const BwdParams &p, cudaStream_t st)
 
 int launch_tf_bwd(const BwdParams &p, cudaStream_t st)
 {
-    if (p.dtype != XFA_F32 || p.drop.on) return XFA_ERR_UNSUPPORTED;
-    if (p.hd == 64) return run<64>(p, st);
-    if (p.hd == 32) return run<32>(p, st);
+    if (p.dtype != XFA_F32) return XFA_ERR_UNSUPPORTED;
+    if (p.hd == 64) return p.drop.on ? run<64, true>(p, st) : run<64, false>(p, st);
+    if (p.hd == 32) return p.drop.on ? run<32, true>(p, st) : run<32, false>(p, st);
     return XFA_ERR_UNSUPPORTED;
 }
 

@@ -21,6 +21,7 @@
 // TMEM (512 columns): Q_hi [0,hd) Q_lo [hd,2hd) S_0 S_1 (64 each) P_lo,0 P_lo,1 (64 each) O (hd).
 #include <math_constants.h>
 
+#include "dropout.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tf32x3.cuh"
@@ -108,10 +109,12 @@ __device__ __forceinline__ void issue_pv(uint32_t o, uint32_t p_hi, uint32_t p_l
     }
 }
 
-template <int HD>
+// DROP: dropout on the probabilities that enter P.V (the row sums l keep every p).
+template <int HD, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     tf_fwd_kernel(const float *__restrict__ Q, const float *__restrict__ K, const float *__restrict__ V,
-                  float *__restrict__ O, float *__restrict__ lse, int bh, int S, float scale_log2, int *status)
+                  float *__restrict__ O, float *__restrict__ lse, int bh, int S, float scale_log2, int *status,
+                  const DropParams drop)
 {
     using C = Cfg<HD>;
     extern __shared__ uint8_t smem_raw[];
@@ -259,6 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         float m = -CUDART_INF_F, l = 0.0f;
         bool ok = true;
+        // dropout: element (row, key) has flat index (head*S + row)*S + key
+        const uint64_t drop_row_g = DROP ? ((uint64_t)head * S + (uint64_t)row) * (uint64_t)S * kDropGolden : 0ull;
         for (int j = 0; j < n; ++j) {
             const int b = j & 1;
             if (!(ok = warp_wait(&bars->s_full[b], (j >> 1) & 1, bars, status))) break;
@@ -305,13 +310,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m = m_new;
             }
             float l4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            uint64_t drop_g = DROP ? drop_row_g + (uint64_t)(j * BN) * kDropGolden : 0ull;
 #pragma unroll
             for (int h = 0; h < BN / 32; ++h) {
                 uint32_t hi[32], lo[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float p = ex2_approx(fmaf(__uint_as_float(s[32 * h + e]), scale_log2, -m));
+                    float p = ex2_approx(fmaf(__uint_as_float(s[32 * h + e]), scale_log2, -m));
                     l4[e & 3] += p;
+                    if (DROP) {
+                        p = drop_keep(drop.seed, drop_g, drop.keep_thr) ? p * drop.inv_keep : 0.0f;
+                        drop_g += kDropGolden;
+                    }
                     split_tf32(p, hi[e], lo[e]);
                 }
                 tmem_st32(tmem + lane_off + C::col_s(b) + 32 * h, hi);
@@ -353,17 +363,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int HD>
+template <int HD, bool DROP>
 int run(const FwdParams &p, cudaStream_t st)
 {
     static_assert(Cfg<HD>::SMEM <= 227 * 1024, "shared memory per CTA");
-    auto kern = tf_fwd_kernel<HD>;
+    auto kern = tf_fwd_kernel<HD, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<HD>::SMEM);
     if (e != cudaSuccess) return XFA_ERR_CUDA_BASE + (int)e;
     const unsigned grid = (unsigned)(((p.S + BM - 1) / BM) * p.bh);
     kern<<<grid, kThreads, Cfg<HD>::SMEM, st>>>((const float *)p.q, (const float *)p.k, (const float *)p.v,
                                                  (float *)p.out, p.lse, p.bh, p.S, p.scale * 1.4426950408889634f,
-                                                 p.status);
+                                                 p.status, p.drop);
     e = cudaGetLastError();
     return e == cudaSuccess ? XFA_OK : XFA_ERR_CUDA_BASE + (int)e;
 }
@@ -372,9 +382,9 @@ int run(const FwdParams &p, cudaStream_t st)
 
 int launch_tf_fwd(const FwdParams &p, cudaStream_t st)
 {
-    if (p.dtype != XFA_F32 || p.drop.on) return XFA_ERR_UNSUPPORTED;
-    if (p.hd == 64) return run<64>(p, st);
-    if (p.hd == 32) return run<32>(p, st);
+    if (p.dtype != XFA_F32) return XFA_ERR_UNSUPPORTED;
+    if (p.hd == 64) return p.drop.on ? run<64, true>(p, st) : run<64, false>(p, st);
+    if (p.hd == 32) return p.drop.on ? run<32, true>(p, st) : run<32, false>(p, st);
     return XFA_ERR_UNSUPPORTED;
 }
 

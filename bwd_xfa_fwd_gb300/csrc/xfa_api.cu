@@ -214,7 +214,6 @@ static int fwd_run(const void *q, const void *k, const void *v, void *out, float
         return XFA_ERR_INVALID_ARG;
     Family fam;
     if ((rc = choose_impl(impl, hd, dtype, &fam)) != XFA_OK) return rc;
-    if (drop.on && fam == Family::Tf32 && impl == XFA_IMPL_AUTO) fam = Family::Simt;   // no fp32 tensor-core dropout
     FwdParams p{q, k, v, out, lse, bh, S, hd, scale, dtype, nullptr};
     p.drop = drop;
     if ((rc = status_ptr(&p.status)) != XFA_OK) return rc;
@@ -357,8 +356,7 @@ static int bwd_run(const void *q, const void *k, const void *v, const void *out,
     p.drop = drop;
     Family fam;
     if ((rc = choose_impl(impl, hd, dtype, &fam)) != XFA_OK) return rc;
-    if (drop.on && fam == Family::Tf32 && impl == XFA_IMPL_AUTO) fam = Family::Simt;   // as in fwd_run
-    if (drop.on && fam == Family::TcDet) return XFA_ERR_UNSUPPORTED;   // dropout: fused and SIMT families only
+    if (drop.on && fam == Family::TcDet) return XFA_ERR_UNSUPPORTED;   // dropout: every family but bf16 TcDet
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if ((rc = stage_prep(p, fam, st)) != XFA_OK) return rc;
     if ((rc = stage_main(p, fam, st)) != XFA_OK) return rc;

@@ -15,7 +15,8 @@ from tests.gpu_helpers import compare, oracle_result, run_gpu, to_device, to_f64
 
 pytestmark = pytest.mark.gpu
 
-FAMILIES = [("bf16", 128, 2), ("bf16", 64, 2), ("bf16", 64, 1), ("f32", 32, 1), ("f32", 64, 1), ("f32", 128, 1)]
+FAMILIES = [("bf16", 128, 2), ("bf16", 64, 2), ("bf16", 64, 1), ("f32", 32, 1), ("f32", 64, 1), ("f32", 128, 1),
+            ("f32", 32, 2), ("f32", 64, 2)]
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -100,13 +100,14 @@ def test_rowdot(dtype, hd):
     assert np.max(np.abs(d - ref)) <= 1e-5 * np.max(np.abs(ref))
 
 
-def test_outputs_do_not_write_outside_their_buffers():
+@pytest.mark.parametrize("dtype,hd", [("bf16", 128), ("f32", 64), ("f32", 32)])
+def test_outputs_do_not_write_outside_their_buffers(dtype, hd):
     """Canary guards around every output buffer stay untouched."""
     from bwd_xfa_fwd_gb300 import binding
-    bh, S, hd = 2, 300, 128
+    bh, S = 2, 300
     scale = 1.0 / math.sqrt(hd)
-    x = inputs.draw((bh, S, hd), "bf16", seed=9)
-    q, k, v, do = (to_device(x[n], "bf16") for n in ("q", "k", "v", "dout"))
+    x = inputs.draw((bh, S, hd), dtype, seed=9)
+    q, k, v, do = (to_device(x[n], dtype) for n in ("q", "k", "v", "dout"))
     n = bh * S * hd
     guard = 4096
 
@@ -115,10 +116,10 @@ def test_outputs_do_not_write_outside_their_buffers():
         return buf, buf[guard:guard + numel]
 
     for impl in (1, 2, 3):
-        bo, out = guarded(n, torch.bfloat16)
+        bo, out = guarded(n, q.dtype)
         bl, lse = guarded(bh * S, torch.float32)
         binding.fwd(q, k, v, scale, impl, out=out.view(bh, S, hd), lse=lse.view(bh, S))
-        grads = [guarded(n, torch.bfloat16) for _ in range(3)]
+        grads = [guarded(n, q.dtype) for _ in range(3)]
         binding.bwd(q, k, v, out.view(bh, S, hd), do, lse.view(bh, S), scale, impl,
                     grads=tuple(g[1].view(bh, S, hd) for g in grads))
         torch.cuda.synchronize()
@@ -141,13 +142,14 @@ def test_backward_is_repeatable_with_reused_workspace():
         assert torch.allclose(s.float(), t.float(), rtol=0, atol=1e-2 * float(s.float().abs().max()))
 
 
-@pytest.mark.parametrize("hd,S", [(128, 1000), (64, 777)])
-def test_deterministic_backward_is_bit_reproducible(hd, S):
-    """XFA_IMPL_TCGEN05_DET forms dQ without atomics: two runs give identical bits."""
+@pytest.mark.parametrize("dtype,hd,S", [("bf16", 128, 1000), ("bf16", 64, 777), ("f32", 64, 777), ("f32", 32, 1000)])
+def test_deterministic_backward_is_bit_reproducible(dtype, hd, S):
+    """XFA_IMPL_TCGEN05_DET (bf16) and the fp32 tensor-core family form dQ without atomics:
+    two runs give identical bits."""
     from bwd_xfa_fwd_gb300 import binding
     bh = 6
-    x = inputs.draw((bh, S, hd), "bf16", seed=31 + hd)
-    q, k, v, do = (to_device(x[n], "bf16") for n in ("q", "k", "v", "dout"))
+    x = inputs.draw((bh, S, hd), dtype, seed=31 + hd)
+    q, k, v, do = (to_device(x[n], dtype) for n in ("q", "k", "v", "dout"))
     out, lse = binding.fwd(q, k, v, impl=binding.IMPL_TCGEN05_DET)
     a = [t.clone() for t in binding.bwd(q, k, v, out, do, lse, impl=binding.IMPL_TCGEN05_DET)]
     for _ in range(2):
@@ -156,13 +158,14 @@ def test_deterministic_backward_is_bit_reproducible(hd, S):
             assert torch.equal(s_, t_)
 
 
-def test_bwd_stages_match_bwd_for_every_impl():
+@pytest.mark.parametrize("dtype,hd", [("bf16", 128), ("f32", 64)])
+def test_bwd_stages_match_bwd_for_every_impl(dtype, hd):
     """prep/main/finish called one by one give what xfa_bwd gives, for each kernel family."""
     from bwd_xfa_fwd_gb300 import binding
-    bh, S, hd = 3, 300, 128
+    bh, S = 3, 300
     scale = 1.0 / math.sqrt(hd)
-    x = inputs.draw((bh, S, hd), "bf16", seed=41)
-    q, k, v, do = (to_device(x[n], "bf16") for n in ("q", "k", "v", "dout"))
+    x = inputs.draw((bh, S, hd), dtype, seed=41)
+    q, k, v, do = (to_device(x[n], dtype) for n in ("q", "k", "v", "dout"))
     for impl in (1, 2, 3):
         out, lse = binding.fwd(q, k, v, scale, impl)
         whole = binding.bwd(q, k, v, out, do, lse, scale, impl)
@@ -174,12 +177,15 @@ def test_bwd_stages_match_bwd_for_every_impl():
             assert torch.allclose(a_.float(), b_.float(), rtol=0, atol=1e-2 * float(a_.float().abs().max()))
 
 
-def test_unsupported_combinations_are_rejected():
+@pytest.mark.parametrize("dtype,hd", [(torch.float32, 128), (torch.bfloat16, 32)])
+def test_unsupported_combinations_are_rejected(dtype, hd):
+    """The tcgen05 families take bf16 with hd 64 / 128 and fp32 (3xTF32) with hd 32 / 64."""
     from bwd_xfa_fwd_gb300 import binding
-    t = torch.zeros(1, 64, 32, device="cuda")
-    with pytest.raises(binding.XfaError) as e:
-        binding.fwd(t, t, t, impl=binding.IMPL_TCGEN05)
-    assert e.value.code == binding.XFA_ERR_UNSUPPORTED
+    t = torch.zeros(1, 64, hd, device="cuda", dtype=dtype)
+    for impl in (binding.IMPL_TCGEN05, binding.IMPL_TCGEN05_DET):
+        with pytest.raises(binding.XfaError) as e:
+            binding.fwd(t, t, t, impl=impl)
+        assert e.value.code == binding.XFA_ERR_UNSUPPORTED
 
 
 def test_timeout_path_reports_and_recovers():
@@ -243,16 +249,17 @@ def _fuzz_cases(n=int(os.environ.get("XFA_FUZZ_CASES", "24")), seed=2024):
     dropout rate comes from a second generator so the other draws stay as they were."""
     rng = np.random.default_rng(seed)
     rng_drop = np.random.default_rng(seed + 1)
+    rng_f32 = np.random.default_rng(seed + 2)   # fp32 kernel family
     cases = []
     for i in range(n):
         dtype = "bf16" if i % 4 else "f32"
         hd = int(rng.choice([64, 128])) if dtype == "bf16" else int(rng.choice([32, 64, 128]))
-        impl = int(rng.choice([0, 2, 3])) if dtype == "bf16" else 1
+        impl = int(rng.choice([0, 2, 3])) if dtype == "bf16" else int(rng_f32.choice([0, 1, 2] if hd < 128 else [0, 1]))
         S = int(rng.integers(1, 1400))
         bh = int(rng.integers(1, 5))
         scale = float(rng.uniform(0.02, 0.3))
         std = float(rng.choice([0.5, 1.0, 2.0, 3.0]))
-        p_drop = float(rng_drop.choice([0.0, 0.0, 0.1, 0.3])) if impl != 3 else 0.0
+        p_drop = float(rng_drop.choice([0.0, 0.0, 0.1, 0.3])) if (dtype, impl) != ("bf16", 3) else 0.0
         cases.append((i, dtype, hd, impl, S, bh, scale, std, p_drop))
     return cases
 
