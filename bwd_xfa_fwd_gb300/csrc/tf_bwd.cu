@@ -92,17 +92,21 @@ __device__ __forceinline__ void mma3(uint32_t d, uint32_t a_hi, uint32_t a_lo, u
 
 // One streamed [BS rows x HD] fp32 tile from global memory (rows past S read as zero) into a
 // K-major hi / lo pair (`khi`, `klo`: HD / 32 blocks of BS rows x 128 B) and, when T, also its
-// transpose (`thi`, `tlo`: HD rows x 128 B, the BS rows contiguous).  128 threads, tid 0..127.
+// transpose (`thi`, `tlo`: HD rows x 128 B, the BS rows contiguous).  128 threads (warp w of the
+// group, lane).  A warp takes 16 consecutive rows x 2 adjacent 16-byte columns: each row's 32
+// bytes are one sector of the global read, and with the 128-byte swizzle both the 16-byte
+// K-major stores and the 4-byte transposed stores of a warp fall in distinct banks.
 template <int HD, bool T>
-__device__ __forceinline__ void split_tile(const float *src, int row0, int S, int tid, uint8_t *khi, uint8_t *klo,
-                                           uint8_t *thi, uint8_t *tlo)
+__device__ __forceinline__ void split_tile(const float *src, int row0, int S, int w, int lane, uint8_t *khi,
+                                           uint8_t *klo, uint8_t *thi, uint8_t *tlo)
 {
     constexpr int F4 = HD / 4;
     constexpr uint32_t BLK = BS * 128;
 #pragma unroll
     for (int it = 0; it < BS * F4 / 128; ++it) {
-        const int idx = it * 128 + tid;
-        const int r = idx / F4, c4 = idx % F4;
+        const int combo = it * 4 + w;                 // (16-row block, column pair)
+        const int r = (combo / (F4 / 2)) * 16 + (lane & 15);
+        const int c4 = (combo % (F4 / 2)) * 2 + (lane >> 4);
         const bool valid = row0 + r < S;
         const float4 x = ldg4_or_zero(src + (size_t)(valid ? row0 + r : 0) * HD + 4 * c4, valid);
         float4 hi, lo;
@@ -210,8 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (i >= NS && !warp_wait(&bars->empty[st], ((i / NS) + 1) & 1, bars, status)) break;
             uint8_t *g = smem + st * C::STAGE;
             const int q0 = k0 + i * BS;
-            split_tile<HD, true>(Q + hoff, q0, S, tid, g + C::OFF_QHI, g + C::OFF_QLO, g + C::OFF_QTHI, g + C::OFF_QTLO);
-            split_tile<HD, true>(dO + hoff, q0, S, tid, g + C::OFF_OHI, g + C::OFF_OLO, g + C::OFF_OTHI,
+            split_tile<HD, true>(Q + hoff, q0, S, w, lane, g + C::OFF_QHI, g + C::OFF_QLO, g + C::OFF_QTHI, g + C::OFF_QTLO);
+            split_tile<HD, true>(dO + hoff, q0, S, w, lane, g + C::OFF_OHI, g + C::OFF_OLO, g + C::OFF_OTHI,
                                  g + C::OFF_OTLO);
             fence_proxy_async_smem();
             __syncwarp();
@@ -403,9 +407,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int st = j % NS;
             if (j >= NS && !warp_wait(&bars->empty[st], ((j / NS) + 1) & 1, bars, status)) break;
             uint8_t *g = smem + st * C::STAGE;
-            split_tile<HD, true>(K + hoff, j * BS, S, tid, g + C::OFF_KHI, g + C::OFF_KLO, g + C::OFF_KTHI,
+            split_tile<HD, true>(K + hoff, j * BS, S, w, lane, g + C::OFF_KHI, g + C::OFF_KLO, g + C::OFF_KTHI,
                                  g + C::OFF_KTLO);
-            split_tile<HD, false>(V + hoff, j * BS, S, tid, g + C::OFF_VHI, g + C::OFF_VLO, nullptr, nullptr);
+            split_tile<HD, false>(V + hoff, j * BS, S, w, lane, g + C::OFF_VHI, g + C::OFF_VLO, nullptr, nullptr);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->full[st]);

@@ -52,11 +52,16 @@ typedef enum { XFA_F32 = 0, XFA_BF16 = 1 } xfa_dtype;
 typedef enum {
     XFA_IMPL_AUTO = 0,        /* the fastest tcgen05 variant where supported, else SIMT */
     XFA_IMPL_SIMT = 1,        /* fp32 FFMA tiled kernels (every dtype and hd) */
-    XFA_IMPL_TCGEN05 = 2,     /* bf16, hd in {64, 128}: TMA + tcgen05.mma + TMEM kernels; the
-                                 backward sums dQ over key tiles with fp32 reductions, so dQ may
-                                 differ in the last bits from run to run */
-    XFA_IMPL_TCGEN05_DET = 3  /* as XFA_IMPL_TCGEN05, but the backward forms dQ in a separate
-                                 query-tile pass without atomics: bit-reproducible results */
+    XFA_IMPL_TCGEN05 = 2,     /* tcgen05.mma + TMEM kernels.  bf16, hd in {64, 128}: TMA-fed
+                                 kernels whose backward sums dQ over key tiles with fp32
+                                 reductions, so dQ may differ in the last bits from run to run.
+                                 fp32, hd in {32, 64}: the 3xTF32 kernels (each operand split
+                                 into two tf32 parts, three MMAs per product, about 2^-21
+                                 relative error per product); their backward forms dQ in a
+                                 query-tile pass without atomics, so results are bit-reproducible */
+    XFA_IMPL_TCGEN05_DET = 3  /* as XFA_IMPL_TCGEN05, but the bf16 backward also forms dQ in a
+                                 separate query-tile pass without atomics: bit-reproducible
+                                 results (fp32: the same kernels as XFA_IMPL_TCGEN05) */
 } xfa_impl;
 
 enum {
@@ -138,7 +143,8 @@ int xfa_bwd_impl(const void *q, const void *k, const void *v, const void *out, c
  *   seed   : 64-bit seed; the forward and the backward of one use must get the
  *            same seed and p_drop.
  * Other arguments as xfa_fwd_impl / xfa_bwd_impl.  Families: XFA_IMPL_AUTO,
- * XFA_IMPL_TCGEN05 (bf16, hd 64 / 128) and XFA_IMPL_SIMT; the backward with
+ * XFA_IMPL_TCGEN05 (bf16 with hd 64 / 128, fp32 with hd 32 / 64) and XFA_IMPL_SIMT;
+ * XFA_IMPL_TCGEN05_DET with fp32 as XFA_IMPL_TCGEN05; the bf16 backward with
  * XFA_IMPL_TCGEN05_DET and p_drop > 0 returns XFA_ERR_UNSUPPORTED.
  */
 int xfa_fwd_dropout(const void *q, const void *k, const void *v, void *out, float *lse,
