@@ -2,7 +2,7 @@
 // (tf_fwd.cu, tf_bwd.cu).
 //
 // An fp32 value x is carried as hi + lo, both rounded to nearest tf32 in software
-// (cvt.rna), so the tensor core reads them unchanged whatever its own handling of fp32
+// (tf32_rna), so the tensor core reads them unchanged whatever its own handling of fp32
 // inputs: hi = tf32(x), lo = tf32(x - hi) (x - hi is exact in fp32), |x - hi - lo| <=
 // 2^-22 |x|.  A product a.b is formed as a_hi.b_hi + a_hi.b_lo + a_lo.b_hi by three
 // kind::tf32 MMAs; the dropped a_lo.b_lo is below 2^-22 |a.b| as well, so each product
@@ -15,12 +15,14 @@
 
 namespace xfa {
 
-// x rounded to the nearest tf32 value (ties away from zero); the low 13 bits come back clear.
+// x rounded to the nearest tf32 value, ties away from zero (the rounding of cvt.rna.tf32.f32),
+// done on the encoding: adding half a tf32 ulp (bit 12) to the magnitude bits and clearing the
+// 13 bits below the tf32 mantissa rounds the magnitude half-up, a carry out of the mantissa
+// steps the exponent, and infinities stay infinite.  Two integer operations instead of a
+// conversion instruction.
 __device__ __forceinline__ float tf32_rna(float x)
 {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
 }
 
 __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo)
