@@ -95,10 +95,53 @@ def dist_env():
         os.environ.get("LOCAL_RANK", "0"))
 
 
+L2_BYTES = 129 * 10**6
+SIMT_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # the SIMT kernels' arithmetic bound
+
+
 def workload_config(w):
+    elt = 2 if w.dtype == "bf16" else 4
+    one = w.bh * w.S * w.hd * elt
+    l2 = (f"inputs (4 x {one / 2**20:.0f} MiB {w.dtype}) larger than L2 (129 MB); no flush" if one > L2_BYTES else
+          f"inputs (4 x {one / 2**20:.2f} MiB {w.dtype}) fit in L2 (129 MB): timed warm, a profiling case")
     return {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "hd": w.hd, "dtype": w.dtype,
-            "scale": w.scale, "causal": True, "layout": "[bh,S,hd] row-major",
-            "l2": "inputs (4 x 64 MiB bf16) larger than L2 (129 MB); no flush"}
+            "scale": w.scale, "causal": True, "layout": "[bh,S,hd] row-major", "l2": l2}
+
+
+def resolved_family(w, family):
+    """The kernel family a call runs: 'tc' (bf16 tcgen05), 'tc_det', 'tf32x3' (fp32 tcgen05)
+    or 'simt' -- as the library's dispatch resolves xfa_impl for this dtype and hd."""
+    if family == "simt":
+        return "simt"
+    if w.dtype == "bf16" and w.hd in (64, 128):
+        return "tc_det" if family == "tcgen05_det" else "tc"
+    if w.dtype == "f32" and w.hd in (32, 64):
+        return "tf32x3"
+    return "simt"
+
+
+def kernel_labels(w, fam):
+    """(forward kernel, backward main-stage kernels, launches per step) of a family."""
+    if fam == "tc":
+        return f"tc_fwd_kernel<{w.hd}>", f"tc_bwd_kernel<{w.hd}>", 4          # fwd, prep, bwd, convert
+    if fam == "tc_det":
+        return f"tc_fwd_kernel<{w.hd}>", f"tc_bwd_kernel<{w.hd}> + tc_dq_kernel<{w.hd}>", 4
+    if fam == "tf32x3":
+        return f"tf_fwd_kernel<{w.hd}>", f"tf_bwd_kv_kernel<{w.hd}> + tf_bwd_q_kernel<{w.hd}>", 4
+    conv = 1 if w.dtype == "bf16" else 0
+    return f"simt_fwd_kernel<{w.dtype},{w.hd}>", f"simt_bwd_kernel<{w.dtype},{w.hd}>", 3 + conv
+
+
+def tensor_peak(pk, pk_kind, fam):
+    """(peak TFLOP/s, source) the family's contractions are measured against.  3xTF32 forms
+    each fp32 product with three tf32 MMAs: its ceiling is the tf32 rate (the measured bf16
+    rate times the nominal dense tf32 / bf16 ratio, 1.1 / 2.25 PFLOP/s) over three."""
+    bf16 = float(pk["bf16_tflops"])
+    if fam == "simt":
+        return SIMT_FMA_TFLOPS, "FFMA: 152 SMs x 128 fp32 FMA/clk x 2 FLOP x 2.07 GHz (maximum SM clock)"
+    if fam == "tf32x3":
+        return bf16 * (1.1 / 2.25) / 3.0, f"{pk_kind} bf16_tflops x nominal tf32/bf16 (1.1/2.25) / 3 MMAs per product"
+    return bf16, f"{pk_kind} bf16_tflops"
 
 
 class ClockSampler:
@@ -371,9 +414,10 @@ def run_ours(args, w):
         e2e = measure_e2e(torch, binding, w, dev, ws, impl, K, f_fwd + f_bwd, world)
 
     pk, pk_kind = peaks()
-    peak_tc = float(pk["bf16_tflops"])
+    rfam = resolved_family(w, args.family)
+    k_fwd, k_bwd, launches = kernel_labels(w, rfam)
+    peak_tc, peak_src = tensor_peak(pk, pk_kind, rfam)
     main_tflops = f_bwd / (per["main"] * 1e-3) / 1e12
-    fam = f"tc_{{}}_kernel<{w.hd}>" if w.dtype == "bf16" else f"simt_{{}}_kernel<{w.dtype},{w.hd}>"
     prep_bytes = w.bh * w.S * (2 * w.hd * 2 + 4 + 4 + 4 + 4 * w.hd)
     line = {
         "metric": METRIC,
@@ -387,35 +431,36 @@ def run_ours(args, w):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": w.dtype,
-        "data": "synthetic (seeded N(0,1), bf16-rounded; recipe in bwd_xfa_fwd_gb300/inputs.py)",
+        "data": ("synthetic (seeded N(0,1)" + (", bf16-rounded" if w.dtype == "bf16" else "")
+                 + "; recipe in bwd_xfa_fwd_gb300/inputs.py)"),
         "config": dict(workload_config(w), kernel_family=args.family,
                        **({"dropout_p": args.dropout, "dropout_seed": DROPOUT_SEED} if args.dropout else {})),
         "fwd_tflops": f_fwd / (per["fwd"] * 1e-3) / 1e12,
         "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
         "fwd_frac_of_peak": f_fwd / (per["fwd"] * 1e-3) / 1e12 / peak_tc,
         "bwd_frac_of_peak": f_bwd / (bwd_ms * 1e-3) / 1e12 / peak_tc,
-        "peak_bf16_tflops": peak_tc,
-        "peak_kind": f"{pk_kind} burst bf16 dense (cuBLAS)",
+        "peak_tensor_tflops": peak_tc,
+        "peak_kind": peak_src,
         "stage_ms": per,
-        "roofline": {"kernel": fam.format("bwd") + (" with its pre-pass and conversion (xfa_bwd_dropout)"
-                                                     if args.dropout else " (xfa_bwd_main)"),
-                     "bound": "tensor", "achieved": main_tflops,
+        "roofline": {"kernel": k_bwd + (" with its pre-pass and conversion (xfa_bwd_dropout)"
+                                        if args.dropout else " (xfa_bwd_main)"),
+                     "bound": "alu" if rfam == "simt" else "tensor", "achieved": main_tflops,
                      "peak": peak_tc, "unit": "TFLOP/s", "frac": main_tflops / peak_tc,
-                     "traffic": (recorded_traffic("tc_bwd", w.name) if w.dtype == "bf16" and not args.dropout
+                     "traffic": (recorded_traffic("tc_bwd", w.name) if rfam == "tc" and not args.dropout
                                  else None),
-                     "peak_source": f"{pk_kind} bf16_tflops"},
-        "roofline_fwd": {"kernel": fam.format("fwd") + " (xfa_fwd)", "bound": "tensor",
+                     "peak_source": peak_src},
+        "roofline_fwd": {"kernel": k_fwd + " (xfa_fwd)", "bound": "alu" if rfam == "simt" else "tensor",
                          "achieved": f_fwd / (per["fwd"] * 1e-3) / 1e12, "peak": peak_tc, "unit": "TFLOP/s",
                          "frac": f_fwd / (per["fwd"] * 1e-3) / 1e12 / peak_tc,
-                         "traffic": (recorded_traffic("tc_fwd", w.name) if w.dtype == "bf16" and not args.dropout
-                                     else None)},
+                         "traffic": (recorded_traffic("tc_fwd", w.name) if rfam in ("tc", "tc_det")
+                                     and not args.dropout else None)},
         "roofline_prep": None if args.dropout else {
             "kernel": "rowdot_kernel (xfa_bwd_prep)", "bound": "hbm",
             "achieved": prep_bytes / (per["prep"] * 1e-3) / 1e9, "peak": float(pk["hbm_gbs"]),
             "unit": "GB/s", "frac": prep_bytes / (per["prep"] * 1e-3) / 1e9 / float(pk["hbm_gbs"]),
             "traffic": recorded_traffic("rowdot", w.name)},
         "e2e": e2e,
-        "gpu_launches": 4 * K,
+        "gpu_launches": launches * K,
         "clocks": clk.result,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -439,14 +484,27 @@ def main():
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="dropout rate on the attention probabilities (0: none, the benchmark's default)")
     ap.add_argument("--family", choices=sorted(FAMILIES), default="auto",
-                    help="kernel family (xfa_impl): auto, tcgen05 (dQ by fp32 reductions), "
-                         "tcgen05_det (dQ by a separate pass, bit-reproducible), simt")
+                    help="kernel family (xfa_impl): auto, tcgen05 (bf16: dQ by fp32 reductions; fp32 with "
+                         "hd 32/64: the 3xTF32 kernels), tcgen05_det (bf16: dQ by a separate pass, "
+                         "bit-reproducible), simt")
     ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=sorted(inputs.WORKLOADS),
                     help="workload id (default: the S=8192 benchmark workload; others for profiling)")
+    ap.add_argument("--shape", default=None,
+                    help="B,H,S,hd,dtype: a seeded synthetic shape of the same recipe instead of --workload "
+                         "(profiling; scale 1/sqrt(hd), seed 0)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = inputs.WORKLOADS[args.workload]
+    if args.shape:
+        try:
+            B, H, S, hd, dt = args.shape.split(",")
+            w = inputs.Workload(f"causal_{dt}_bh{int(B) * int(H)}_s{int(S)}_hd{int(hd)}", int(B), int(H), int(S),
+                                int(hd), dt, 1.0 / math.sqrt(int(hd)), seed=0)
+        except ValueError:
+            ap.error("--shape wants B,H,S,hd,dtype (dtype f32 or bf16)")
+        if w.dtype not in ("f32", "bf16"):
+            ap.error("--shape dtype must be f32 or bf16")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

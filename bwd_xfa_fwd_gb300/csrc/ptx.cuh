@@ -236,31 +236,6 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
-// kind::tf32: D[tmem] (+)= A[tmem] * B[smem]  (A: M lanes x K fp32 elements, one per column;
-// B: K-major, 128-byte rows of 32 elements).
-__device__ __forceinline__ void mma_ts_tf32(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// kind::tf32: D[tmem] (+)= A[smem] * B[smem]^T  (both K-major, 128-byte rows of 32 elements).
-__device__ __forceinline__ void mma_ss_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // One lane of a converged warp is elected (elect.sync); returns true in that lane only.
 __device__ __forceinline__ bool elect_one()
 {
@@ -282,16 +257,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
            | (1u << 10)                    // B format: bf16
            | ((a_mn ? 1u : 0u) << 15)      // A major
            | ((b_mn ? 1u : 0u) << 16)      // B major
-           | ((uint32_t)(N >> 3) << 17)    // N / 8
-           | ((uint32_t)(M >> 4) << 24);   // M / 16
-}
-
-// Instruction descriptor of kind::tf32 with K-major tf32 A/B and an fp32 accumulator.
-__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N)
-{
-    return (1u << 4)                       // D format: f32
-           | (2u << 7)                     // A format: tf32
-           | (2u << 10)                    // B format: tf32
            | ((uint32_t)(N >> 3) << 17)    // N / 8
            | ((uint32_t)(M >> 4) << 24);   // M / 16
 }

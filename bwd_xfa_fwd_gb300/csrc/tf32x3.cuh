@@ -38,6 +38,41 @@ __device__ __forceinline__ void split4(const float4 &x, float4 &hi, float4 &lo)
     lo = make_float4(tf32_rna(x.x - hi.x), tf32_rna(x.y - hi.y), tf32_rna(x.z - hi.z), tf32_rna(x.w - hi.w));
 }
 
+// kind::tf32: D[tmem] (+)= A[tmem] * B[smem]  (A: M lanes x K fp32 elements, one per column;
+// B: K-major, 128-byte rows of 32 elements).
+__device__ __forceinline__ void mma_ts_tf32(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// kind::tf32: D[tmem] (+)= A[smem] * B[smem]^T  (both K-major, 128-byte rows of 32 elements).
+__device__ __forceinline__ void mma_ss_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor of kind::tf32 with K-major tf32 A/B and an fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N)
+{
+    return (1u << 4)                       // D format: f32
+           | (2u << 7)                     // A format: tf32
+           | (2u << 10)                    // B format: tf32
+           | ((uint32_t)(N >> 3) << 17)    // N / 8
+           | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a tile of 128-byte rows with
 // the 128-byte swizzle (chunk index XOR row mod 8; tile base 1024-byte aligned).  A K-major
 // tcgen05 operand of 32-bit elements holds 32 of them per row.
