@@ -78,6 +78,32 @@ def recorded_traffic(name, workload):
     return e["dram_bytes_per_launch"]
 
 
+def measure_graph(torch, step, K, flops):
+    """The same step captured once in a CUDA graph and replayed K times: the library neither
+    allocates nor synchronises, so a whole forward + backward is capturable, and replaying
+    it removes the per-call host cost that dominates small problems."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()                       # warm on a side stream before capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(K):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / K
+    return {"ms_per_step": ms, "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "replays": K}
+
+
 def max_over_ranks(value: float, device=None) -> float:
     """The largest `value` over all ranks of the default process group (the
     value itself when no group is initialised)."""
@@ -404,6 +430,8 @@ def run_ours(args, w):
     f_fwd, f_bwd = w.fwd_flops(), w.bwd_flops()
     bwd_ms = per["prep"] + per["main"] + per["finish"]
 
+    graph = measure_graph(torch, step, K, f_fwd + f_bwd) if args.graph else None
+
     # End to end through the C ABI with host buffers.  Every step copies its inputs
     # (Q, K, V, dO) from pinned host memory to the device and reads O, L, dQ, dK, dV
     # back into pinned host memory.  Steps are software-pipelined over three streams
@@ -460,6 +488,7 @@ def run_ours(args, w):
             "unit": "GB/s", "frac": prep_bytes / (per["prep"] * 1e-3) / 1e9 / float(pk["hbm_gbs"]),
             "traffic": recorded_traffic("rowdot", w.name)},
         "e2e": e2e,
+        "graph": graph,
         "gpu_launches": launches * K,
         "clocks": clk.result,
     }
@@ -489,6 +518,8 @@ def main():
                          "bit-reproducible), simt")
     ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=sorted(inputs.WORKLOADS),
                     help="workload id (default: the S=8192 benchmark workload; others for profiling)")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step captured in a CUDA graph and replayed (added as \"graph\")")
     ap.add_argument("--shape", default=None,
                     help="B,H,S,hd,dtype: a seeded synthetic shape of the same recipe instead of --workload "
                          "(profiling; scale 1/sqrt(hd), seed 0)")

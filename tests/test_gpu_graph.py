@@ -1,0 +1,67 @@
+"""A whole forward + backward captured in a CUDA graph and replayed (GB300 only).  The library
+neither allocates nor synchronises inside a call (the caller passes every buffer and the
+workspace), so the calls are capturable; replays must reproduce the eager results."""
+import math
+
+import pytest
+import torch
+
+from bwd_xfa_fwd_gb300 import inputs
+from tests.gpu_helpers import to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from bwd_xfa_fwd_gb300 import binding, build
+    build.build()
+    binding.load()
+    assert torch.cuda.is_available()
+
+
+# (dtype, hd, impl, bit-exact): the families without atomics replay bit for bit
+CASES = [("f32", 64, 2, True), ("f32", 32, 2, True), ("bf16", 128, 3, True), ("bf16", 64, 3, True),
+         ("bf16", 128, 2, False), ("f32", 64, 1, False)]
+
+
+@pytest.mark.parametrize("dtype,hd,impl,exact", CASES)
+def test_graph_replay_matches_eager(dtype, hd, impl, exact):
+    from bwd_xfa_fwd_gb300 import binding
+    bh, S = 3, 333
+    scale = 1.0 / math.sqrt(hd)
+    x = inputs.draw((bh, S, hd), dtype, seed=88 + hd)
+    q, k, v, do = (to_device(x[n], dtype) for n in ("q", "k", "v", "dout"))
+    out = torch.empty_like(q)
+    lse = torch.empty(bh, S, device="cuda", dtype=torch.float32)
+    grads = tuple(torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(binding.workspace_bytes(bh, S, hd, q.dtype), device="cuda", dtype=torch.uint8)
+
+    def step():
+        binding.fwd(q, k, v, scale, impl, out=out, lse=lse)
+        binding.bwd(q, k, v, out, do, lse, scale, impl, workspace=ws, grads=grads)
+
+    step()
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in (out, lse) + grads]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(2):
+        for t in (out, lse) + grads:
+            t.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert binding.status() == binding.XFA_OK
+        for a, b in zip(eager, (out, lse) + grads):
+            if exact:
+                assert torch.equal(a, b)
+            else:   # dQ summed with atomics in a data-dependent order (bf16: one rounding step apart)
+                tol = (1e-2 if dtype == "bf16" else 1e-5) * float(a.float().abs().max())
+                assert torch.allclose(a.float(), b.float(), rtol=0, atol=tol)
