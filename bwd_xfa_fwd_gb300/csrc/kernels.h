@@ -52,6 +52,17 @@ struct BwdParams {
 // Rows of D / Lg are padded to a multiple of this.
 constexpr int kRowPad = 128;
 
+// Heads a tensor-core kernel schedules together.  Long sequences go in bundles of `dflt`
+// heads, longest work first within a bundle, so that the operands of the heads in flight stay
+// in L2; when four [bh, S, hd] operands fit in 64 MiB (a fraction of the 129 MB L2) the whole
+// grid is one bundle, i.e. longest work first across all heads, which packs the waves of a
+// short-sequence grid best.
+inline int head_bundle(int bh, int S, int hd, int elt_bytes, int dflt)
+{
+    const double bytes = 4.0 * (double)bh * (double)S * (double)hd * (double)elt_bytes;
+    return bytes <= 64.0 * 1024.0 * 1024.0 ? bh : dflt;
+}
+
 // SIMT (FFMA) family: any dtype, hd in {32, 64, 128}.
 cudaError_t launch_simt_fwd(const FwdParams &p, cudaStream_t st);
 cudaError_t launch_simt_bwd(const BwdParams &p, cudaStream_t st);

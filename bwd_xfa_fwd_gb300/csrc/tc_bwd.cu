@@ -48,7 +48,7 @@ template <int HD>
 constexpr int ring_depth() { return HD == 128 ? 3 : 4; }   // query-tile (Q, dO, L, D) ring stages
 constexpr int kThreads = 320;
 constexpr int kWarpTma = 8, kWarpMma = 9;
-constexpr int kHeadBundle = 4;   // heads scheduled together (L2 reuse of inputs and dQ accumulator)
+constexpr int kHeadBundle = 4;   // heads scheduled together at long S (L2 reuse of inputs and dQ accumulator)
 
 template <int HD>
 struct Cfg {
@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                   const float *__restrict__ Lg, const float *__restrict__ Dg, float *__restrict__ dq_acc,
                   __nv_bfloat16 *__restrict__ dK, __nv_bfloat16 *__restrict__ dV, int bh, int S, int S_pad,
-                  float scale, float scale_log2, int *status, const DropParams drop)
+                  float scale, float scale_log2, int *status, const DropParams drop, int bundle_heads)
 {
     using C = Cfg<HD>;
     constexpr int NSQ = C::NSQ;
@@ -191,14 +191,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *dq_stage = reinterpret_cast<float *>(smem + C::OFF_DQ);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    // Work order: heads in bundles of kHeadBundle (so the inputs and the dQ accumulator of the
-    // heads in flight stay in L2), and within a bundle the key tiles with the most query tiles first.
+    // Work order: heads in bundles of bundle_heads (see head_bundle: at long S the inputs and the
+    // dQ accumulator of the heads in flight stay in L2), and within a bundle the key tiles with the
+    // most query tiles first.
     const int nkt = (S + BN - 1) / BN;
-    const int bundle = (int)blockIdx.x / (nkt * kHeadBundle);
-    const int g = min(kHeadBundle, bh - bundle * kHeadBundle);
-    const int idx = (int)blockIdx.x - bundle * nkt * kHeadBundle;
+    const int bundle = (int)blockIdx.x / (nkt * bundle_heads);
+    const int g = min(bundle_heads, bh - bundle * bundle_heads);
+    const int idx = (int)blockIdx.x - bundle * nkt * bundle_heads;
     const int jt = idx / g;
-    const int head = bundle * kHeadBundle + idx % g;
+    const int head = bundle * bundle_heads + idx % g;
     const int j0 = jt * BN;
     const int nq_total = (S + BM - 1) / BM;
     const int it0 = (j0 / BM);                    // first query tile at or below the diagonal
@@ -590,7 +591,8 @@ int run(const BwdParams &p, cudaStream_t st)
     const unsigned grid = (unsigned)(nkt * p.bh);
     kern<<<grid, kThreads, Cfg<HD>::SMEM, st>>>(tk, tv, tq, tdo, tdk, tdv, p.Lg, p.D, p.dq_acc, (__nv_bfloat16 *)p.dk,
                                                  (__nv_bfloat16 *)p.dv, p.bh, p.S, p.S_pad, p.scale,
-                                                 p.scale * 1.4426950408889634f, p.status, p.drop);
+                                                 p.scale * 1.4426950408889634f, p.status, p.drop,
+                                                 head_bundle(p.bh, p.S, HD, 2, kHeadBundle));
     e = cudaGetLastError();
     return e == cudaSuccess ? XFA_OK : XFA_ERR_CUDA_BASE + (int)e;
 }

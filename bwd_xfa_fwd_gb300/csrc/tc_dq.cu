@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const float *__restrict__ Lg, const float *__restrict__ Dg, __nv_bfloat16 *__restrict__ dQ, int bh,
-                 int S, int S_pad, float scale, float scale_log2, int *status)
+                 int S, int S_pad, float scale, float scale_log2, int *status, int bundle_heads)
 {
     using C = Cfg<HD>;
     static_assert(sizeof(Bars) <= 256, "barrier block");
@@ -96,13 +96,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     Bars *bars = reinterpret_cast<Bars *>(smem + C::OFF_BAR);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    // heads in bundles, longest query tiles first within a bundle
+    // heads in bundles of bundle_heads (see head_bundle), longest query tiles first within a bundle
     const int nqt = (S + BM - 1) / BM;
-    const int bundle = (int)blockIdx.x / (nqt * kHeadBundle);
-    const int g = min(kHeadBundle, bh - bundle * kHeadBundle);
-    const int idx = (int)blockIdx.x - bundle * nqt * kHeadBundle;
+    const int bundle = (int)blockIdx.x / (nqt * bundle_heads);
+    const int g = min(bundle_heads, bh - bundle * bundle_heads);
+    const int idx = (int)blockIdx.x - bundle * nqt * bundle_heads;
     const int qt = nqt - 1 - idx / g;
-    const int head = bundle * kHeadBundle + idx % g;
+    const int head = bundle * bundle_heads + idx % g;
     const int q0 = qt * BM;
     const int nkv = qt + 1;   // key tiles 0..qt (tile qt holds the diagonal)
 
@@ -321,7 +321,8 @@ int run(const BwdParams &p, cudaStream_t st)
     const int nqt = (p.S + BM - 1) / BM;
     kern<<<(unsigned)(nqt * p.bh), kThreads, Cfg<HD>::SMEM, st>>>(tq, tdo, tk, tv, p.Lg, p.D,
                                                                    (__nv_bfloat16 *)p.dq, p.bh, p.S, p.S_pad, p.scale,
-                                                                   p.scale * 1.4426950408889634f, p.status);
+                                                                   p.scale * 1.4426950408889634f, p.status,
+                                                                   head_bundle(p.bh, p.S, HD, 2, kHeadBundle));
     e = cudaGetLastError();
     return e == cudaSuccess ? XFA_OK : XFA_ERR_CUDA_BASE + (int)e;
 }

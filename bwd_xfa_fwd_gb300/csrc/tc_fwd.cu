@@ -39,7 +39,7 @@ constexpr int kThreads = 320;         // 10 warps
 constexpr int kWarpTma = 8, kWarpMma = 9;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
-constexpr int kHeadBundle = 8;              // heads scheduled together (L2 reuse of K/V)
+constexpr int kHeadBundle = 8;              // heads scheduled together at long S (L2 reuse of K/V)
 
 template <int HD>
 struct Cfg {
@@ -128,7 +128,8 @@ template <int HD, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ O,
-                  float *__restrict__ lse, int bh, int S, float scale_log2, int *status, const DropParams drop)
+                  float *__restrict__ lse, int bh, int S, float scale_log2, int *status, const DropParams drop,
+                  int bundle_heads)
 {
     using C = Cfg<HD>;
     extern __shared__ uint8_t smem_raw[];
@@ -136,14 +137,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     Bars *bars = reinterpret_cast<Bars *>(smem + C::OFF_BAR);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    // Work order: heads in bundles of kHeadBundle (so the K/V of the heads in flight stay in
-    // L2), and within a bundle the heaviest (longest) query blocks first.
+    // Work order: heads in bundles of bundle_heads (see head_bundle: at long S the K/V of the
+    // heads in flight stay in L2), and within a bundle the heaviest (longest) query blocks first.
     const int nqb = (S + 2 * BM - 1) / (2 * BM);
-    const int bundle = (int)blockIdx.x / (nqb * kHeadBundle);
-    const int g = min(kHeadBundle, bh - bundle * kHeadBundle);   // heads in this bundle
-    const int idx = (int)blockIdx.x - bundle * nqb * kHeadBundle;
+    const int bundle = (int)blockIdx.x / (nqb * bundle_heads);
+    const int g = min(bundle_heads, bh - bundle * bundle_heads);   // heads in this bundle
+    const int idx = (int)blockIdx.x - bundle * nqb * bundle_heads;
     const int qb = nqb - 1 - idx / g;
-    const int head = bundle * kHeadBundle + idx % g;
+    const int head = bundle * bundle_heads + idx % g;
     const int q0 = qb * 2 * BM;
     const bool t1 = q0 + BM < S;
     const int n_t0 = 2 * qb + 1, n_t1 = t1 ? 2 * qb + 2 : 0;   // key tiles per query tile
@@ -420,7 +421,8 @@ int run(const FwdParams &p, cudaStream_t st)
     const int nqb = (p.S + 2 * BM - 1) / (2 * BM);
     const unsigned grid = (unsigned)(nqb * p.bh);
     kern<<<grid, kThreads, Cfg<HD>::SMEM, st>>>(tq, tk, tv, (__nv_bfloat16 *)p.out, p.lse, p.bh, p.S,
-                                                 p.scale * 1.4426950408889634f, p.status, p.drop);
+                                                 p.scale * 1.4426950408889634f, p.status, p.drop,
+                                                 head_bundle(p.bh, p.S, HD, 2, kHeadBundle));
     e = cudaGetLastError();
     return e == cudaSuccess ? XFA_OK : XFA_ERR_CUDA_BASE + (int)e;
 }

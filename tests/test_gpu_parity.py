@@ -64,6 +64,20 @@ def test_workload_full_size_sampled(wid, heads, impl):
     _identities(got, x, w.dtype)
 
 
+@pytest.mark.parametrize("hd,S", [(64, 4096), (32, 6000)])
+def test_f32_tensor_core_long_sequence_sampled(hd, S):
+    """The 3xTF32 family at long sequences (many key tiles per query tile, a ragged tail at
+    S = 6000): sampled heads against the oracle, the exact identities on every head."""
+    bh = 4
+    scale = 1.0 / math.sqrt(hd)
+    x = inputs.draw((bh, S, hd), "f32", seed=4242 + hd, stds=(1.0, 1.0, 1.0, 1.0))
+    got = run_gpu(x, "f32", scale, impl=2)
+    heads = (0, 3)
+    ref = oracle_result(("f32long", hd, S), x, scale, heads=list(heads))
+    compare(got, ref, "f32", heads=heads)
+    _identities(got, x, "f32")
+
+
 RAGGED = [1, 5, 64, 100, 128, 129, 255, 256, 257, 300, 511, 777]
 
 
