@@ -91,6 +91,9 @@ int launch_tf_fwd(const FwdParams &p, cudaStream_t st);
 // dK, dV by key tiles, then dQ by query tiles (no atomics); writes p.dq / p.dk / p.dv.
 int launch_tf_bwd(const BwdParams &p, cudaStream_t st);
 
+// Streaming multiprocessors of the current device (queried once per device), for persistent grids.
+int device_sm_count();
+
 // Encodes the TMA descriptors; resolved once from the driver (xfa_api.cu).
 int encode_tmap_bf16_3d(void *tmap, const void *base, int hd, int S, int bh, int box_rows);
 

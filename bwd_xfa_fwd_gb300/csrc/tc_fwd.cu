@@ -23,6 +23,9 @@
 //     in TMEM after the previous P.V has completed (guaranteed by the S-ready
 //     commit, which tracks every earlier MMA).
 // TMEM map (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+hd) O1 [256+hd, 256+2hd).
+#include <algorithm>
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -60,11 +63,15 @@ struct Cfg {
 
 struct Bars {
     uint64_t q_full;
+    uint64_t q_empty;     // the item's last S MMAs have read Q (tensor-core commit)
     uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
     uint64_t s_full[2];   // S_t ready in TMEM (tensor-core commit)
     uint64_t p_full[2];   // P_t written to TMEM (one arrival per softmax warp)
     uint64_t o_full[2];   // O_t complete (commit after the last P.V)
     uint64_t drain;       // MMA drain at teardown
+    uint64_t item_full[2];   // work-item id posted by the TMA warp
+    uint64_t item_empty[2];  // id read by the MMA warp and the eight softmax warps
+    int item_id[2];          // the posted ids (-1: no more work)
     uint32_t tmem_base;
     int abort;
 };
@@ -83,6 +90,19 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, Bars *
     ok = __all_sync(0xffffffffu, ok);
     if (!ok && (threadIdx.x & 31) == 0) fail(b, status);
     return ok;
+}
+
+// The next work item for a consumer warp (MMA or softmax): waits until the TMA warp has posted
+// it in ring entry k & 1, reads it and releases the entry (one arrival per warp).  -1: no more
+// work, or the wait gave up (then ok is false).
+__device__ __forceinline__ int take_item(Bars *b, int k, int *status, bool &ok)
+{
+    const int e = k & 1;
+    if (!(ok = warp_wait(&b->item_full[e], (k >> 1) & 1, b, status))) return -1;
+    const int item = *reinterpret_cast<volatile int *>(&b->item_id[e]);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&b->item_empty[e]);
+    return item;
 }
 
 // S = Q K^T: M=128, N=128, K=hd in steps of 16 (K-major, 128-byte swizzle; 64-column blocks SUB_BYTES apart).
@@ -129,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ O,
                   float *__restrict__ lse, int bh, int S, float scale_log2, int *status, const DropParams drop,
-                  int bundle_heads)
+                  int bundle_heads, unsigned *__restrict__ next_item)
 {
     using C = Cfg<HD>;
     extern __shared__ uint8_t smem_raw[];
@@ -137,21 +157,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     Bars *bars = reinterpret_cast<Bars *>(smem + C::OFF_BAR);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    // Work order: heads in bundles of bundle_heads (see head_bundle: at long S the K/V of the
-    // heads in flight stay in L2), and within a bundle the heaviest (longest) query blocks first.
+    // Persistent CTAs: the grid has at most one CTA per SM, and each CTA takes work items -- query
+    // blocks of 256 rows (two tiles) of one head -- from a shared counter (next_item, zeroed
+    // before the launch) until the list is exhausted: greedy scheduling, as the hardware does
+    // for a grid of one CTA per item, without the CTA teardown and launch between items.  The
+    // list runs heads in bundles of bundle_heads (see head_bundle: at long S the K/V of the
+    // heads in flight stay in L2) and, within a bundle, the heaviest (longest) query blocks
+    // first.  The TMA warp claims an item and posts its id to the other warps through a
+    // two-entry ring; barrier phases and the K/V ring carry over from one item to the next: the
+    // next item's Q loads as soon as the current item's last S MMA has read the old one, and its
+    // first S MMAs run while the softmax warps still write out the current item's O.
     const int nqb = (S + 2 * BM - 1) / (2 * BM);
-    const int bundle = (int)blockIdx.x / (nqb * bundle_heads);
-    const int g = min(bundle_heads, bh - bundle * bundle_heads);   // heads in this bundle
-    const int idx = (int)blockIdx.x - bundle * nqb * bundle_heads;
-    const int qb = nqb - 1 - idx / g;
-    const int head = bundle * bundle_heads + idx % g;
-    const int q0 = qb * 2 * BM;
-    const bool t1 = q0 + BM < S;
-    const int n_t0 = 2 * qb + 1, n_t1 = t1 ? 2 * qb + 2 : 0;   // key tiles per query tile
-    const int nkv = t1 ? n_t1 : n_t0;
+    const int n_items = nqb * bh;
+    auto item_coords = [&](int item, int &head, int &qb) {
+        const int bundle = item / (nqb * bundle_heads);
+        const int g = min(bundle_heads, bh - bundle * bundle_heads);   // heads in this bundle
+        const int idx = item - bundle * nqb * bundle_heads;
+        qb = nqb - 1 - idx / g;
+        head = bundle * bundle_heads + idx % g;
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->q_empty, 1);
         for (int s = 0; s < 3; ++s) {
             mbar_init(&bars->k_full[s], 1);
             mbar_init(&bars->k_empty[s], 1);
@@ -164,6 +192,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->o_full[t], 1);
         }
         mbar_init(&bars->drain, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->item_full[i], 1);
+            mbar_init(&bars->item_empty[i], 1 + BM / 32 * 2);   // MMA warp + eight softmax warps
+        }
         bars->abort = 0;
         fence_barrier_init();
     }
@@ -181,38 +213,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
-            int issued[3] = {0, 0, 0};
-            mbar_arrive_expect_tx(&bars->q_full, (t1 ? 2 : 1) * C::TILE_BYTES);
-            for (int s = 0; s < C::SUB; ++s) {
-                tma_load_3d(smem + C::OFF_Q0 + s * C::SUB_BYTES, &tm_q, &bars->q_full, s * 64, q0, head);
-                if (t1) tma_load_3d(smem + C::OFF_Q1 + s * C::SUB_BYTES, &tm_q, &bars->q_full, s * 64, q0 + BM, head);
-            }
-            for (int j = 0; j < nkv; ++j) {
-                const int st = j % C::NS;
-                const uint32_t ph = ((j / C::NS) + 1) & 1;   // parity of the release of the previous use
-                if (j >= C::NS && !mbar_wait(&bars->k_empty[st], ph, &bars->abort)) { fail(bars, status); break; }
-                mbar_arrive_expect_tx(&bars->k_full[st], C::TILE_BYTES);
-                for (int s = 0; s < C::SUB; ++s)
-                    tma_load_3d(smem + C::OFF_K + st * C::TILE_BYTES + s * C::SUB_BYTES, &tm_k, &bars->k_full[st],
-                                s * 64, j * BN, head);
-                if (j >= C::NS && !mbar_wait(&bars->v_empty[st], ph, &bars->abort)) {
-                    issued[st] = j + 1;   // K of round j was issued
-                    fail(bars, status);
-                    break;
+            uint32_t g = 0;                       // K/V tiles issued by this CTA
+            uint32_t last_k[3] = {0, 0, 0}, last_v[3] = {0, 0, 0};   // 1 + last tile issued per stage
+            int k = 0;                            // items whose Q was issued
+            bool ok = true;
+            for (int kc = 0; ok; ++kc) {          // kc: items claimed, posted in ring entry kc & 1
+                const int e = kc & 1;
+                if (kc >= 2 && !(ok = mbar_wait(&bars->item_empty[e], ((kc >> 1) + 1) & 1, &bars->abort))) break;
+                int item = (int)atomicAdd(next_item, 1u);
+                if (item >= n_items) item = -1;
+                *reinterpret_cast<volatile int *>(&bars->item_id[e]) = item;
+                mbar_arrive(&bars->item_full[e]);
+                if (item < 0) break;
+                int head, qb;
+                item_coords(item, head, qb);
+                const int q0 = qb * 2 * BM;
+                const bool t1 = q0 + BM < S;
+                const int nkv = t1 ? 2 * qb + 2 : 2 * qb + 1;
+                // the Q buffers are free once the previous item's last S MMAs have read them
+                if (k > 0 && !(ok = mbar_wait(&bars->q_empty, (k - 1) & 1, &bars->abort))) break;
+                mbar_arrive_expect_tx(&bars->q_full, (t1 ? 2 : 1) * C::TILE_BYTES);
+                for (int s = 0; s < C::SUB; ++s) {
+                    tma_load_3d(smem + C::OFF_Q0 + s * C::SUB_BYTES, &tm_q, &bars->q_full, s * 64, q0, head);
+                    if (t1) tma_load_3d(smem + C::OFF_Q1 + s * C::SUB_BYTES, &tm_q, &bars->q_full, s * 64, q0 + BM, head);
                 }
-                mbar_arrive_expect_tx(&bars->v_full[st], C::TILE_BYTES);
-                for (int s = 0; s < C::SUB; ++s)
-                    tma_load_3d(smem + C::OFF_V + st * C::TILE_BYTES + s * C::SUB_BYTES, &tm_v, &bars->v_full[st],
-                                s * 64, j * BN, head);
-                issued[st] = j + 1;
+                ++k;
+                for (int j = 0; j < nkv; ++j, ++g) {
+                    const int st = g % C::NS;
+                    const uint32_t ph = ((g / C::NS) + 1) & 1;   // parity of the release of the previous use
+                    if (g >= C::NS && !(ok = mbar_wait(&bars->k_empty[st], ph, &bars->abort))) break;
+                    mbar_arrive_expect_tx(&bars->k_full[st], C::TILE_BYTES);
+                    for (int s = 0; s < C::SUB; ++s)
+                        tma_load_3d(smem + C::OFF_K + st * C::TILE_BYTES + s * C::SUB_BYTES, &tm_k, &bars->k_full[st],
+                                    s * 64, j * BN, head);
+                    last_k[st] = g + 1;
+                    if (g >= C::NS && !(ok = mbar_wait(&bars->v_empty[st], ph, &bars->abort))) break;
+                    mbar_arrive_expect_tx(&bars->v_full[st], C::TILE_BYTES);
+                    for (int s = 0; s < C::SUB; ++s)
+                        tma_load_3d(smem + C::OFF_V + st * C::TILE_BYTES + s * C::SUB_BYTES, &tm_v, &bars->v_full[st],
+                                    s * 64, j * BN, head);
+                    last_v[st] = g + 1;
+                }
             }
-            // Never leave the CTA with copies in flight: wait for the last load of each stage.
-            mbar_wait(&bars->q_full, 0, nullptr);
+            if (!ok) fail(bars, status);
+            // Never leave the CTA with copies in flight: wait for the last load of Q and of each stage.
+            if (k > 0) mbar_wait(&bars->q_full, (k - 1) & 1, nullptr);
             for (int st = 0; st < C::NS; ++st) {
-                if (issued[st] == 0) continue;
-                const uint32_t ph = ((issued[st] - 1) / C::NS) & 1;
-                mbar_wait(&bars->k_full[st], ph, nullptr);
-                mbar_wait(&bars->v_full[st], ph, nullptr);
+                if (last_k[st]) mbar_wait(&bars->k_full[st], ((last_k[st] - 1) / C::NS) & 1, nullptr);
+                if (last_v[st]) mbar_wait(&bars->v_full[st], ((last_v[st] - 1) / C::NS) & 1, nullptr);
             }
         }
     } else if (warp == kWarpMma) {
@@ -223,57 +271,78 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     sdesc_sw128(smem_u32(smem + C::OFF_Q1), 16, 1024)};
         const uint64_t k_desc = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);
         const uint64_t v_desc = sdesc_sw128(smem_u32(smem + C::OFF_V), C::SUB_BYTES, 1024);
-        bool ok = warp_wait(&bars->q_full, 0, bars, status) && warp_wait(&bars->k_full[0], 0, bars, status);
-        if (ok) {
+        uint32_t g = 0;                 // K/V tiles consumed by this CTA
+        uint32_t np[2] = {0, 0};        // P phases consumed per tile
+        int k = 0;                      // items started
+        bool ok = true;
+        for (; ok; ++k) {
+            const int item = take_item(bars, k, status, ok);
+            if (item < 0) break;
+            int head, qb;
+            item_coords(item, head, qb);
+            const int q0 = qb * 2 * BM;
+            const bool t1 = q0 + BM < S;
+            const int n_t0 = 2 * qb + 1, n_t1 = t1 ? 2 * qb + 2 : 0;
+            const int nkv = t1 ? n_t1 : n_t0;
+            const int st0 = g % C::NS;
+            ok = warp_wait(&bars->q_full, k & 1, bars, status) &&
+                 warp_wait(&bars->k_full[st0], (g / C::NS) & 1, bars, status);
+            if (!ok) break;
             tc_fence_after_sync();
             if (leader) {
-                issue_qk<HD>(tmem + C::col_s(0), q_desc[0], k_desc);
+                // S_0 of both tiles.  Each S buffer last held the previous item's final P, read by
+                // its last P.V issued before: the tensor pipe runs in order.
+                issue_qk<HD>(tmem + C::col_s(0), q_desc[0], sdesc_advance(k_desc, st0 * C::TILE_BYTES));
                 tc_commit(&bars->s_full[0]);
                 if (t1) {
-                    issue_qk<HD>(tmem + C::col_s(1), q_desc[1], k_desc);
+                    issue_qk<HD>(tmem + C::col_s(1), q_desc[1], sdesc_advance(k_desc, st0 * C::TILE_BYTES));
                     tc_commit(&bars->s_full[1]);
                 }
-                tc_commit(&bars->k_empty[0]);
+                tc_commit(&bars->k_empty[st0]);
+                if (nkv == 1) tc_commit(&bars->q_empty);   // no further S of this item reads Q
             }
             __syncwarp();
-        }
-        for (int j = 0; ok && j < nkv; ++j) {
-            const int st = j % C::NS;
-            const uint32_t ph = (j / C::NS) & 1;
-            bool v_ready = false, k_next_ready = false;
-            const int jn = j + 1, stn = jn % C::NS;
-            const uint32_t phn = (jn / C::NS) & 1;
+            for (int j = 0; ok && j < nkv; ++j) {
+                const uint32_t gj = g + j, gn = gj + 1;
+                const int st = gj % C::NS, stn = gn % C::NS;
+                const uint32_t ph = (gj / C::NS) & 1, phn = (gn / C::NS) & 1;
+                bool v_ready = false, k_next_ready = false;
+                const int jn = j + 1;
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const int nt = t == 0 ? n_t0 : n_t1;
-                if (j >= nt) continue;
-                ok = warp_wait(&bars->p_full[t], j & 1, bars, status);
-                if (ok && !v_ready) ok = v_ready = warp_wait(&bars->v_full[st], ph, bars, status);
-                if (!ok) break;
-                tc_fence_after_sync();
-                if (leader) {
-                    issue_pv<HD>(tmem + C::col_o(t), tmem + C::col_s(t), sdesc_advance(v_desc, st * C::TILE_BYTES),
-                                 j > 0);
-                    if (j == nt - 1) tc_commit(&bars->o_full[t]);
-                }
-                __syncwarp();
-                if (jn < nt) {
-                    if (!k_next_ready) ok = k_next_ready = warp_wait(&bars->k_full[stn], phn, bars, status);
+                for (int t = 0; t < 2; ++t) {
+                    const int nt = t == 0 ? n_t0 : n_t1;
+                    if (j >= nt) continue;
+                    ok = warp_wait(&bars->p_full[t], np[t] & 1, bars, status);
+                    ++np[t];
+                    if (ok && !v_ready) ok = v_ready = warp_wait(&bars->v_full[st], ph, bars, status);
                     if (!ok) break;
                     tc_fence_after_sync();
                     if (leader) {
-                        issue_qk<HD>(tmem + C::col_s(t), q_desc[t], sdesc_advance(k_desc, stn * C::TILE_BYTES));
-                        tc_commit(&bars->s_full[t]);
+                        issue_pv<HD>(tmem + C::col_o(t), tmem + C::col_s(t), sdesc_advance(v_desc, st * C::TILE_BYTES),
+                                     j > 0);
+                        if (j == nt - 1) tc_commit(&bars->o_full[t]);
                     }
                     __syncwarp();
+                    if (jn < nt) {
+                        if (!k_next_ready) ok = k_next_ready = warp_wait(&bars->k_full[stn], phn, bars, status);
+                        if (!ok) break;
+                        tc_fence_after_sync();
+                        if (leader) {
+                            issue_qk<HD>(tmem + C::col_s(t), q_desc[t], sdesc_advance(k_desc, stn * C::TILE_BYTES));
+                            tc_commit(&bars->s_full[t]);
+                        }
+                        __syncwarp();
+                    }
                 }
+                if (!ok) break;
+                if (leader) {
+                    if (k_next_ready) tc_commit(&bars->k_empty[stn]);
+                    tc_commit(&bars->v_empty[st]);
+                    if (jn == nkv - 1) tc_commit(&bars->q_empty);   // the item's last S MMAs are issued
+                }
+                __syncwarp();
             }
-            if (!ok) break;
-            if (leader) {
-                if (k_next_ready) tc_commit(&bars->k_empty[stn]);
-                tc_commit(&bars->v_empty[st]);
-            }
-            __syncwarp();
+            g += nkv;
         }
         if (leader) {
             tc_commit(&bars->drain);
@@ -284,117 +353,131 @@ __global__ void __launch_bounds__(kThreads, 1)
         // softmax group of tile t; thread = query row
         const int t = warp / 4, wq = warp % 4;
         const int r = wq * 32 + lane;               // row within the tile == TMEM lane
-        const int row = q0 + t * BM + r;
-        const int diag = 2 * qb + t;                // key tile that holds this tile's diagonal
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem + lane_off + C::col_s(t);
         const uint32_t tO = tmem + lane_off + C::col_o(t);
-        float m = -CUDART_INF_F, l = 0.0f;
+        uint32_t ns = 0, no = 0;                    // S and O phases of this tile consumed
         bool ok = true;
-        const uint64_t drop_row_g = DROP ? ((uint64_t)head * S + (uint64_t)row) * (uint64_t)S * kDropGolden : 0ull;
-        const int n_mine = t == 0 ? n_t0 : n_t1;
-        for (int j = 0; j < n_mine; ++j) {
-            if (!(ok = warp_wait(&bars->s_full[t], j & 1, bars, status))) break;
-            tc_fence_after_sync();
-            // pass 1: row maximum, the scores read from TMEM in two 64-column halves (so only half
-            // a row is held in registers); the diagonal tile masks keys past the row.  4 independent
-            // chains of 3-input maxima.
-            const bool on_diag = j == diag;
-            float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+        for (int k = 0; ok; ++k) {
+            const int item = take_item(bars, k, status, ok);
+            if (item < 0) break;
+            int head, qb;
+            item_coords(item, head, qb);
+            const int q0 = qb * 2 * BM;
+            const bool t1 = q0 + BM < S;
+            if (t == 1 && !t1) continue;                // this item has no second tile
+            const int n_mine = t == 0 ? 2 * qb + 1 : 2 * qb + 2;
+            const int row = q0 + t * BM + r;
+            const int diag = 2 * qb + t;                // key tile that holds this tile's diagonal
+            float m = -CUDART_INF_F, l = 0.0f;
+            const uint64_t drop_row_g = DROP ? ((uint64_t)head * S + (uint64_t)row) * (uint64_t)S * kDropGolden : 0ull;
+            for (int j = 0; j < n_mine; ++j) {
+                if (!(ok = warp_wait(&bars->s_full[t], ns & 1, bars, status))) break;
+                ++ns;
+                tc_fence_after_sync();
+                // pass 1: row maximum, the scores read from TMEM in two 64-column halves (so only half
+                // a row is held in registers); the diagonal tile masks keys past the row.  4 independent
+                // chains of 3-input maxima.
+                const bool on_diag = j == diag;
+                float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t sh[64];
-                load_scores_half(tS, h, on_diag, r, sh);
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t sh[64];
+                    load_scores_half(tS, h, on_diag, r, sh);
 #pragma unroll
-                for (int c = 0; c < 64; c += 8)
+                    for (int c = 0; c < 64; c += 8)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        mx4[e] = fmax3(mx4[e], __uint_as_float(sh[c + 2 * e]), __uint_as_float(sh[c + 2 * e + 1]));
-            }
-            const float mx = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
-            const float m_new = fmaxf(m, mx * scale_log2);   // scale > 0: max commutes with the scaling
-            const bool need = m_new > m + kRescaleThreshold;
-            if (__any_sync(0xffffffffu, need)) {
-                const float alpha = ex2_approx(m - m_new);   // 0 on the first tile
-                l *= alpha;
-                if (j > 0) {
+                        for (int e = 0; e < 4; ++e)
+                            mx4[e] = fmax3(mx4[e], __uint_as_float(sh[c + 2 * e]), __uint_as_float(sh[c + 2 * e + 1]));
+                }
+                const float mx = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
+                const float m_new = fmaxf(m, mx * scale_log2);   // scale > 0: max commutes with the scaling
+                const bool need = m_new > m + kRescaleThreshold;
+                if (__any_sync(0xffffffffu, need)) {
+                    const float alpha = ex2_approx(m - m_new);   // 0 on the first tile
+                    l *= alpha;
+                    if (j > 0) {
 #pragma unroll 1
-                    for (int c = 0; c < HD; c += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(tO + c, o);
-                        tmem_wait_ld();
-                        reg_fence32(o);
+                        for (int c = 0; c < HD; c += 32) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + c, o);
+                            tmem_wait_ld();
+                            reg_fence32(o);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(tO + c, o);
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tmem_st32(tO + c, o);
+                        }
+                        tmem_wait_st();
                     }
-                    tmem_wait_st();
+                    m = m_new;
                 }
-                m = m_new;
-            }
-            // p = 2^(s * scale * log2(e) - m): packed FFMA pairs + ex2; 4 packed partial row sums
-            const uint64_t c2 = f2_pack(scale_log2, scale_log2);
-            const uint64_t nm2 = f2_pack(-m, -m);
-            uint64_t l2[4] = {0ull, 0ull, 0ull, 0ull};
-            // pass 2: the exponentials, half a row at a time (the scores read again)
+                // p = 2^(s * scale * log2(e) - m): packed FFMA pairs + ex2; 4 packed partial row sums
+                const uint64_t c2 = f2_pack(scale_log2, scale_log2);
+                const uint64_t nm2 = f2_pack(-m, -m);
+                uint64_t l2[4] = {0ull, 0ull, 0ull, 0ull};
+                // pass 2: the exponentials, half a row at a time (the scores read again)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t sh[64];
-                load_scores_half(tS, h, on_diag, r, sh);
-                uint32_t pk[32];
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t sh[64];
+                    load_scores_half(tS, h, on_diag, r, sh);
+                    uint32_t pk[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int c = 64 * h + 2 * e;
-                    const float2 a = f2_unpack(ffma2(f2_pack(__uint_as_float(sh[2 * e]), __uint_as_float(sh[2 * e + 1])), c2, nm2));
-                    const float p0 = ex2_approx(a.x);
-                    const float p1 = ex2_approx(a.y);
-                    l2[e & 3] = fadd2(l2[e & 3], f2_pack(p0, p1));
-                    if (DROP) {
-                        // keys j*BN + c, c + 1 of this row: flat index (head*S + row)*S + key
-                        const uint64_t g0 = drop_row_g + (uint64_t)(j * BN + c) * kDropGolden;
-                        const float d0 = drop_keep(drop.seed, g0, drop.keep_thr) ? p0 * drop.inv_keep : 0.0f;
-                        const float d1 =
-                            drop_keep(drop.seed, g0 + kDropGolden, drop.keep_thr) ? p1 * drop.inv_keep : 0.0f;
-                        pk[e] = pack_bf16x2(d0, d1);
-                    } else {
-                        pk[e] = pack_bf16x2(p0, p1);
+                    for (int e = 0; e < 32; ++e) {
+                        const int c = 64 * h + 2 * e;
+                        const float2 a = f2_unpack(ffma2(f2_pack(__uint_as_float(sh[2 * e]), __uint_as_float(sh[2 * e + 1])), c2, nm2));
+                        const float p0 = ex2_approx(a.x);
+                        const float p1 = ex2_approx(a.y);
+                        l2[e & 3] = fadd2(l2[e & 3], f2_pack(p0, p1));
+                        if (DROP) {
+                            // keys j*BN + c, c + 1 of this row: flat index (head*S + row)*S + key
+                            const uint64_t g0 = drop_row_g + (uint64_t)(j * BN + c) * kDropGolden;
+                            const float d0 = drop_keep(drop.seed, g0, drop.keep_thr) ? p0 * drop.inv_keep : 0.0f;
+                            const float d1 =
+                                drop_keep(drop.seed, g0 + kDropGolden, drop.keep_thr) ? p1 * drop.inv_keep : 0.0f;
+                            pk[e] = pack_bf16x2(d0, d1);
+                        } else {
+                            pk[e] = pack_bf16x2(p0, p1);
+                        }
                     }
+                    tmem_st32(tS + 32 * h, pk);
                 }
-                tmem_st32(tS + 32 * h, pk);
+                {
+                    const float2 a = f2_unpack(fadd2(fadd2(l2[0], l2[1]), fadd2(l2[2], l2[3])));
+                    l += a.x + a.y;
+                }
+                tmem_wait_st();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->p_full[t]);
             }
+            if (!ok) break;
+            if (!(ok = warp_wait(&bars->o_full[t], no & 1, bars, status))) break;
+            ++no;
             {
-                const float2 a = f2_unpack(fadd2(fadd2(l2[0], l2[1]), fadd2(l2[2], l2[3])));
-                l += a.x + a.y;
-            }
-            tmem_wait_st();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->p_full[t]);
-        }
-        if (ok && n_mine > 0 && warp_wait(&bars->o_full[t], 0, bars, status)) {
-            tc_fence_after_sync();
-            const float inv_l = 1.0f / l;
-            __nv_bfloat16 *orow = O + ((size_t)head * S + row) * HD;
+                tc_fence_after_sync();
+                const float inv_l = 1.0f / l;
+                __nv_bfloat16 *orow = O + ((size_t)head * S + row) * HD;
 #pragma unroll 1
-            for (int c = 0; c < HD; c += 32) {
-                uint32_t o[32];
-                tmem_ld32(tO + c, o);
-                tmem_wait_ld();
-                reg_fence32(o);
-                if (row < S) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+                for (int c = 0; c < HD; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c, o);
+                    tmem_wait_ld();
+                    reg_fence32(o);
+                    if (row < S) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
-                        w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
-                        w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
-                        w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
-                        dst[v] = w;
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
+                            w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
+                            w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
+                            w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
+                            dst[v] = w;
+                        }
                     }
                 }
+                if (row < S) lse[(size_t)head * S + row] = (m + __log2f(l)) * kLn2;
             }
-            if (row < S) lse[(size_t)head * S + row] = (m + __log2f(l)) * kLn2;
         }
     }
 
@@ -404,6 +487,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         tmem_dealloc(tmem, 512);
     }
+}
+
+// Work-item counters of the persistent forward: one slot per launch, handed out round-robin so
+// that launches in flight on different streams use different slots, and zeroed on the launch's
+// stream just before it (a memset node when the launch is captured in a graph).
+constexpr int kSchedSlots = 64;
+__device__ unsigned g_next_item[kSchedSlots];
+std::atomic<unsigned> g_next_slot{0};
+
+int next_item_counter(cudaStream_t st, unsigned **ctr)
+{
+    void *base = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&base, g_next_item);
+    if (e != cudaSuccess) return XFA_ERR_CUDA_BASE + (int)e;
+    *ctr = static_cast<unsigned *>(base) + g_next_slot.fetch_add(1u) % kSchedSlots;
+    e = cudaMemsetAsync(*ctr, 0, sizeof(unsigned), st);
+    return e == cudaSuccess ? XFA_OK : XFA_ERR_CUDA_BASE + (int)e;
 }
 
 template <int HD, bool DROP>
@@ -419,10 +519,12 @@ int run(const FwdParams &p, cudaStream_t st)
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<HD>::SMEM);
     if (e != cudaSuccess) return XFA_ERR_CUDA_BASE + (int)e;
     const int nqb = (p.S + 2 * BM - 1) / (2 * BM);
-    const unsigned grid = (unsigned)(nqb * p.bh);
+    const unsigned grid = (unsigned)std::min(nqb * p.bh, device_sm_count());   // persistent: one CTA per SM
+    unsigned *ctr = nullptr;
+    if ((rc = next_item_counter(st, &ctr)) != XFA_OK) return rc;
     kern<<<grid, kThreads, Cfg<HD>::SMEM, st>>>(tq, tk, tv, (__nv_bfloat16 *)p.out, p.lse, p.bh, p.S,
                                                  p.scale * 1.4426950408889634f, p.status, p.drop,
-                                                 head_bundle(p.bh, p.S, HD, 2, kHeadBundle));
+                                                 head_bundle(p.bh, p.S, HD, 2, kHeadBundle), ctr);
     e = cudaGetLastError();
     return e == cudaSuccess ? XFA_OK : XFA_ERR_CUDA_BASE + (int)e;
 }

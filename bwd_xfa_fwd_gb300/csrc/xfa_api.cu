@@ -68,6 +68,8 @@ bool device_is_sm103()
     return g_is_sm103[dev] == 1;
 }
 
+int g_sm_count[kMaxDevices];   // 0 unknown
+
 bool aligned16(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int validate_shape(int bh, int S, int hd, float scale, int dtype)
@@ -149,6 +151,19 @@ int resolve_encoder()
 }
 
 }  // namespace
+
+int device_sm_count()
+{
+    int dev;
+    if (current_device(&dev) != XFA_OK) return 1;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sm_count[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
 
 // [bh][S][hd] bf16 tensor as a 3-D TMA map with boxes of 64 columns x box_rows rows,
 // 128-byte swizzle; rows past S read as zero.
