@@ -35,6 +35,9 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <algorithm>
+#include <atomic>
+
 #include "dropout.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -88,6 +91,9 @@ struct Bars {
     uint64_t q_full[kMaxRing], q_empty[kMaxRing];
     uint64_t s_full[2], p_full, ds_full[2], ds_empty[2];
     uint64_t kt_full, dp_full, dq_full, dq_empty, done, drain;
+    uint64_t dk_read;                      // the readout warps have read the item's dK out of TMEM
+    uint64_t item_full[2], item_empty[2];  // work-item ids posted by the TMA warp, read by the others
+    int item_id[2];                        // the posted ids (-1: no more work)
     uint32_t tmem_base;
     int abort;
 };
@@ -106,15 +112,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, Bars *
     return ok;
 }
 
-// Epilogue of one 128-row accumulator (dK or dV): thread r (TMEM lane r) converts its row of
-// hd fp32 columns to bf16 and writes it into `stage`, laid out as the 128-byte-swizzled TMA box
-// ([hd / 64][128 rows][128 B], 16-byte chunk c of row r at chunk c ^ (r & 7)); once the 128
-// threads of the group (named barrier `bar_id`) are through, `issuer` stores the tile with TMA
-// (rows past the tensor's extent are not written) and waits until the stores have read the
-// staging tile; their writes complete before the grid does.
+// Epilogue of one 128-row accumulator (dK or dV) straight to global memory: thread = row of the
+// key tile (TMEM lane), its hd fp32 columns converted to bf16 and written as 16-byte stores; rows
+// past S are not written.
 template <int HD>
-__device__ __forceinline__ void store_rows_tma(uint32_t t_row, uint8_t *stage, int r, const CUtensorMap *map, int y,
-                                               int z, uint32_t bar_id, bool issuer)
+__device__ __forceinline__ void store_rows_global(uint32_t t_row, __nv_bfloat16 *dst, bool valid)
 {
 #pragma unroll 1
     for (int c = 0; c < HD; c += 32) {
@@ -122,26 +124,32 @@ __device__ __forceinline__ void store_rows_tma(uint32_t t_row, uint8_t *stage, i
         tmem_ld32(t_row + c, o);
         tmem_wait_ld();
         reg_fence32(o);
-        uint8_t *row = stage + (c / 64) * (128 * 128) + r * 128;
+        if (valid) {
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]), __uint_as_float(o[8 * v + 1]));
-            w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]), __uint_as_float(o[8 * v + 3]));
-            w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]), __uint_as_float(o[8 * v + 5]));
-            w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]), __uint_as_float(o[8 * v + 7]));
-            const int chunk = (c % 64) / 8 + v;
-            *reinterpret_cast<uint4 *>(row + ((chunk ^ (r & 7)) << 4)) = w;
+            for (int v = 0; v < 4; ++v) {
+                uint4 w;
+                w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]), __uint_as_float(o[8 * v + 1]));
+                w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]), __uint_as_float(o[8 * v + 3]));
+                w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]), __uint_as_float(o[8 * v + 5]));
+                w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]), __uint_as_float(o[8 * v + 7]));
+                d4[v] = w;
+            }
         }
     }
-    fence_proxy_async_smem();
-    named_bar_sync(bar_id, 128);
-    if (issuer) {
-#pragma unroll
-        for (int s = 0; s < HD / 64; ++s) tma_store_3d(map, stage + s * 128 * 128, s * 64, y, z);
-        bulk_commit_group();
-        bulk_wait_group_read0();
-    }
+}
+
+// The next work item for a consumer warp: waits until the TMA warp has posted it in ring entry
+// k & 1, reads it and releases the entry (one arrival per warp).  -1: no more work, or the
+// wait gave up (then ok is false).
+__device__ __forceinline__ int take_item(Bars *b, int k, int *status, bool &ok)
+{
+    const int e = k & 1;
+    if (!(ok = warp_wait(&b->item_full[e], (k >> 1) & 1, b, status))) return -1;
+    const int item = *reinterpret_cast<volatile int *>(&b->item_id[e]);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&b->item_empty[e]);
+    return item;
 }
 
 // C[M=128, N=64] = A[128 rows x hd] * B[64 rows x hd]^T, both K-major (hd contiguous);
@@ -176,10 +184,10 @@ template <int HD, bool FUSED_DQ, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-                  const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                   const float *__restrict__ Lg, const float *__restrict__ Dg, float *__restrict__ dq_acc,
                   __nv_bfloat16 *__restrict__ dK, __nv_bfloat16 *__restrict__ dV, int bh, int S, int S_pad,
-                  float scale, float scale_log2, int *status, const DropParams drop, int bundle_heads)
+                  float scale, float scale_log2, int *status, const DropParams drop, int bundle_heads,
+                  unsigned *__restrict__ next_item)
 {
     using C = Cfg<HD>;
     constexpr int NSQ = C::NSQ;
@@ -191,19 +199,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *dq_stage = reinterpret_cast<float *>(smem + C::OFF_DQ);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    // Work order: heads in bundles of bundle_heads (see head_bundle: at long S the inputs and the
-    // dQ accumulator of the heads in flight stay in L2), and within a bundle the key tiles with the
-    // most query tiles first.
+    // Persistent CTAs: at most one per SM, each taking work items -- the 128 keys of one key tile
+    // of one head -- from a shared counter (next_item, zeroed before the launch) until the list
+    // is exhausted: greedy scheduling without a CTA teardown and launch between items.  The list
+    // runs heads in bundles of bundle_heads (see head_bundle: at long S the inputs and the dQ
+    // accumulator of the heads in flight stay in L2) and, within a bundle, the key tiles with the
+    // most query tiles first.  The TMA warp claims an item and posts its id to the other warps
+    // through a two-entry ring.  Every per-tile barrier phase, ring stage and dS buffer follows
+    // the CTA's running count of query tiles (gi), so the query ring streams on from one item into
+    // the next; K and V of the next item load once the current item's MMAs are done with them.
     const int nkt = (S + BN - 1) / BN;
-    const int bundle = (int)blockIdx.x / (nkt * bundle_heads);
-    const int g = min(bundle_heads, bh - bundle * bundle_heads);
-    const int idx = (int)blockIdx.x - bundle * nkt * bundle_heads;
-    const int jt = idx / g;
-    const int head = bundle * bundle_heads + idx % g;
-    const int j0 = jt * BN;
+    const int n_items = nkt * bh;
     const int nq_total = (S + BM - 1) / BM;
-    const int it0 = (j0 / BM);                    // first query tile at or below the diagonal
-    const int n = nq_total - it0;                 // >= 1
+    struct Item {
+        int head, j0, it0, n;   // head, first key, first query tile at or below the diagonal, tiles
+    };
+    auto item_of = [&](int item) {
+        const int bundle = item / (nkt * bundle_heads);
+        const int g = min(bundle_heads, bh - bundle * bundle_heads);
+        const int idx = item - bundle * nkt * bundle_heads;
+        Item w;
+        w.head = bundle * bundle_heads + idx % g;
+        w.j0 = (idx / g) * BN;
+        w.it0 = w.j0 / BM;
+        w.n = nq_total - w.it0;   // >= 1
+        return w;
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->kv_full, 1);
@@ -214,6 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars->ds_full[b], 4);   // one arrival per key warp
             mbar_init(&bars->ds_empty[b], 1);
+            mbar_init(&bars->item_full[b], 1);
+            mbar_init(&bars->item_empty[b], 9);   // MMA warp, four key warps, four readout warps
         }
         mbar_init(&bars->s_full[0], 1);
         mbar_init(&bars->s_full[1], 1);
@@ -223,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->dq_full, 1);
         mbar_init(&bars->dq_empty, HD / 32);   // one arrival per readout warp
         mbar_init(&bars->done, 1);
+        mbar_init(&bars->dk_read, 4);         // one arrival per readout warp
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         fence_barrier_init();
@@ -242,34 +266,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tensormap(&tm_v);
             prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_do);
-            mbar_arrive_expect_tx(&bars->kv_full, 2 * C::KV_BYTES);
-            for (int s = 0; s < C::SUB; ++s) {
-                tma_load_3d(smem + C::OFF_K + s * C::KV_SUB, &tm_k, &bars->kv_full, s * 64, j0, head);
-                tma_load_3d(smem + C::OFF_V + s * C::KV_SUB, &tm_v, &bars->kv_full, s * 64, j0, head);
-            }
-            int issued[NSQ] = {};
-            for (int it = 0; it < n; ++it) {
-                const int st = it % NSQ;
-                if (it >= NSQ && !mbar_wait(&bars->q_empty[st], ((it / NSQ) + 1) & 1, &bars->abort)) {
-                    fail(bars, status);
-                    break;
-                }
-                const int i0 = (it0 + it) * BM;
-                mbar_arrive_expect_tx(&bars->q_full[st], 2 * C::Q_BYTES + 2 * BM * 4);
+            uint32_t gt = 0;                      // query tiles issued
+            uint32_t last[kMaxRing] = {};         // 1 + last tile issued per stage
+            int kv_loads = 0;
+            bool ok = true;
+            for (int kc = 0; ok; ++kc) {          // kc: items claimed, posted in ring entry kc & 1
+                const int e = kc & 1;
+                if (kc >= 2 && !(ok = mbar_wait(&bars->item_empty[e], ((kc >> 1) + 1) & 1, &bars->abort))) break;
+                int item = (int)atomicAdd(next_item, 1u);
+                if (item >= n_items) item = -1;
+                *reinterpret_cast<volatile int *>(&bars->item_id[e]) = item;
+                mbar_arrive(&bars->item_full[e]);
+                if (item < 0) break;
+                const Item w = item_of(item);
+                // K, V of this item: their buffers are free once the previous item's MMAs are done
+                if (kc > 0 && !(ok = mbar_wait(&bars->done, (kc - 1) & 1, &bars->abort))) break;
+                mbar_arrive_expect_tx(&bars->kv_full, 2 * C::KV_BYTES);
                 for (int s = 0; s < C::SUB; ++s) {
-                    tma_load_3d(smem + C::OFF_Q + st * C::Q_BYTES + s * C::Q_SUB, &tm_q, &bars->q_full[st], s * 64,
-                                i0, head);
-                    tma_load_3d(smem + C::OFF_DO + st * C::Q_BYTES + s * C::Q_SUB, &tm_do, &bars->q_full[st],
-                                s * 64, i0, head);
+                    tma_load_3d(smem + C::OFF_K + s * C::KV_SUB, &tm_k, &bars->kv_full, s * 64, w.j0, w.head);
+                    tma_load_3d(smem + C::OFF_V + s * C::KV_SUB, &tm_v, &bars->kv_full, s * 64, w.j0, w.head);
                 }
-                float *ld = ld_s + st * 2 * BM;
-                bulk_load(ld, Lg + (size_t)head * S_pad + i0, BM * 4, &bars->q_full[st]);
-                bulk_load(ld + BM, Dg + (size_t)head * S_pad + i0, BM * 4, &bars->q_full[st]);
-                issued[st] = it + 1;
+                ++kv_loads;
+                for (int it = 0; it < w.n; ++it) {
+                    const uint32_t gi = gt + it;
+                    const int st = gi % NSQ;
+                    if (gi >= NSQ && !(ok = mbar_wait(&bars->q_empty[st], ((gi / NSQ) + 1) & 1, &bars->abort))) break;
+                    const int i0 = (w.it0 + it) * BM;
+                    mbar_arrive_expect_tx(&bars->q_full[st], 2 * C::Q_BYTES + 2 * BM * 4);
+                    for (int s = 0; s < C::SUB; ++s) {
+                        tma_load_3d(smem + C::OFF_Q + st * C::Q_BYTES + s * C::Q_SUB, &tm_q, &bars->q_full[st],
+                                    s * 64, i0, w.head);
+                        tma_load_3d(smem + C::OFF_DO + st * C::Q_BYTES + s * C::Q_SUB, &tm_do, &bars->q_full[st],
+                                    s * 64, i0, w.head);
+                    }
+                    float *ld = ld_s + st * 2 * BM;
+                    bulk_load(ld, Lg + (size_t)w.head * S_pad + i0, BM * 4, &bars->q_full[st]);
+                    bulk_load(ld + BM, Dg + (size_t)w.head * S_pad + i0, BM * 4, &bars->q_full[st]);
+                    last[st] = gi + 1;
+                }
+                gt += w.n;
             }
-            mbar_wait(&bars->kv_full, 0, nullptr);
+            if (!ok) fail(bars, status);
+            // Never leave the CTA with copies in flight: wait for the last load of K/V and of each stage.
+            if (kv_loads > 0) mbar_wait(&bars->kv_full, (kv_loads - 1) & 1, nullptr);
             for (int st = 0; st < NSQ; ++st)
-                if (issued[st]) mbar_wait(&bars->q_full[st], ((issued[st] - 1) / NSQ) & 1, nullptr);
+                if (last[st]) mbar_wait(&bars->q_full[st], ((last[st] - 1) / NSQ) & 1, nullptr);
         }
     } else if (warp == kWarpMma) {
         // The whole warp runs the issue loop (converged, descriptors warp-uniform);
@@ -288,279 +329,321 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idesc_acc = idesc_bf16(BN, HD, false, true);    // dV, dK: B MN-major
         constexpr uint32_t idesc_dq = idesc_bf16(128, BM, true, true);     // dQ^T: A, B MN-major
         constexpr uint32_t idesc_s = idesc_bf16(BN, BM, false, false);     // S^T: A = K_j from TMEM
-        bool ok = warp_wait(&bars->kv_full, 0, bars, status) && warp_wait(&bars->kt_full, 0, bars, status) &&
-                  warp_wait(&bars->q_full[0], 0, bars, status);
-        if (ok) {
+        uint32_t gt = 0;   // query tiles of earlier items
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const int item = take_item(bars, k, status, ok);
+            if (item < 0) break;
+            const int n = item_of(item).n;
+            const int st0 = gt % NSQ;
+            ok = warp_wait(&bars->kv_full, k & 1, bars, status) && warp_wait(&bars->kt_full, k & 1, bars, status) &&
+                 warp_wait(&bars->q_full[st0], (gt / NSQ) & 1, bars, status);
+            if (!ok) break;
             tc_fence_after_sync();
             if (leader) {
-                issue_s<HD>(tmem + C::COL_S, tmem + C::COL_KT, q_km, idesc_s);
-                tc_commit(&bars->s_full[0]);
-                issue_rows_dot<HD>(tmem + C::COL_DP, v_km, do_km);
+                // the S^T / dP^T columns last held the previous item's final P^T / dS^T, read by
+                // its dV / dK MMAs issued before (in order)
+                issue_s<HD>(tmem + C::col_s(!FUSED_DQ, gt), tmem + C::COL_KT,
+                            sdesc_advance(q_km, st0 * C::Q_BYTES), idesc_s);
+                tc_commit(&bars->s_full[FUSED_DQ ? 0 : (gt & 1)]);
+                issue_rows_dot<HD>(tmem + C::COL_DP, v_km, sdesc_advance(do_km, st0 * C::Q_BYTES));
                 tc_commit(&bars->dp_full);
             }
             __syncwarp();
-        }
-        for (int it = 0; ok && it < n; ++it) {
-            const int b = it & 1, st = it % NSQ;
-            const uint32_t ph2 = (it >> 1) & 1;
-            const uint32_t qoff = st * C::Q_BYTES, dsoff = b * C::DS_BYTES;
-            const int nx = it + 1, stn = nx % NSQ;
-            // Next S^T.  Without the fused dQ it goes first, into the other S^T buffer, so that it
-            // does not queue behind this tile's work (that buffer's P^T, tile it - 1, was read by
-            // the dV MMA issued one iteration ago, and the in-order pipe runs that MMA first).
-            // With one buffer it follows this tile's dV, which reads P^T from the same columns.
-            const bool s_first = !FUSED_DQ && nx < n;
-            if (s_first) {
-                if (!(ok = warp_wait(&bars->q_full[stn], (nx / NSQ) & 1, bars, status))) break;
+            for (int it = 0; ok && it < n; ++it) {
+                const uint32_t gi = gt + it;
+                const int b = gi & 1, st = gi % NSQ;
+                const uint32_t ph2 = (gi >> 1) & 1;
+                const uint32_t qoff = st * C::Q_BYTES, dsoff = b * C::DS_BYTES;
+                const int nx = it + 1;
+                const uint32_t gn = gi + 1;
+                const int stn = gn % NSQ;
+                // Next S^T.  Without the fused dQ it goes first, into the other S^T buffer, so that it
+                // does not queue behind this tile's work (that buffer's P^T, tile gi - 1, was read by
+                // the dV MMA issued one iteration ago, and the in-order pipe runs that MMA first).
+                // With one buffer it follows this tile's dV, which reads P^T from the same columns.
+                const bool s_first = !FUSED_DQ && nx < n;
+                if (s_first) {
+                    if (!(ok = warp_wait(&bars->q_full[stn], (gn / NSQ) & 1, bars, status))) break;
+                    tc_fence_after_sync();
+                    if (leader) {
+                        issue_s<HD>(tmem + C::col_s(true, gn), tmem + C::COL_KT, sdesc_advance(q_km, stn * C::Q_BYTES),
+                                    idesc_s);
+                        tc_commit(&bars->s_full[gn & 1]);
+                    }
+                    __syncwarp();
+                }
+                // dV += P^T dO_i  (P^T: bf16 in the first columns of this tile's S^T).  The item's
+                // first dV overwrites the accumulator, which the key warps have read out before
+                // they wrote this P^T.
+                if (!(ok = warp_wait(&bars->p_full, gi & 1, bars, status))) break;
                 tc_fence_after_sync();
                 if (leader) {
-                    issue_s<HD>(tmem + C::col_s(true, nx), tmem + C::COL_KT, sdesc_advance(q_km, stn * C::Q_BYTES),
-                                idesc_s);
-                    tc_commit(&bars->s_full[nx & 1]);
+#pragma unroll
+                    for (int ks = 0; ks < BM / 16; ++ks)
+                        mma_ts(tmem + C::COL_DV, tmem + C::col_s(!FUSED_DQ, gi) + ks * 8,
+                               sdesc_advance(do_mn, qoff + ks * 2048), idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
                 }
                 __syncwarp();
-            }
-            // dV += P^T dO_i  (P^T: bf16 in the first columns of this tile's S^T)
-            if (!(ok = warp_wait(&bars->p_full, it & 1, bars, status))) break;
-            tc_fence_after_sync();
-            if (leader) {
+                if (FUSED_DQ && nx < n) {   // next S^T: its columns are free once the dV MMA above has read P^T
+                    if (!(ok = warp_wait(&bars->q_full[stn], (gn / NSQ) & 1, bars, status))) break;
+                    tc_fence_after_sync();
+                    if (leader) {
+                        issue_s<HD>(tmem + C::COL_S, tmem + C::COL_KT, sdesc_advance(q_km, stn * C::Q_BYTES), idesc_s);
+                        tc_commit(&bars->s_full[0]);
+                    }
+                    __syncwarp();
+                }
+                // dS^T is in TMEM (first columns of dP^T) and in smem: dK first (reads the TMEM copy),
+                // then the next dP^T may overwrite those columns.  The item's first dK overwrites the
+                // accumulator: the readout warps must have read the previous item's dK out of it.
+                if (!(ok = warp_wait(&bars->ds_full[b], ph2, bars, status))) break;
+                if (it == 0 && k > 0 && !(ok = warp_wait(&bars->dk_read, (k - 1) & 1, bars, status))) break;
+                tc_fence_after_sync();
+                if (leader) {
 #pragma unroll
-                for (int ks = 0; ks < BM / 16; ++ks)
-                    mma_ts(tmem + C::COL_DV, tmem + C::col_s(!FUSED_DQ, it) + ks * 8,
-                           sdesc_advance(do_mn, qoff + ks * 2048), idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
+                    for (int ks = 0; ks < BM / 16; ++ks)
+                        mma_ts(tmem + C::COL_DK, tmem + C::COL_DP + ks * 8, sdesc_advance(q_mn, qoff + ks * 2048),
+                               idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
+                    tc_commit(&bars->q_empty[st]);
+                    if (nx < n) {
+                        issue_rows_dot<HD>(tmem + C::COL_DP, v_km, sdesc_advance(do_km, stn * C::Q_BYTES));
+                        tc_commit(&bars->dp_full);
+                    }
+                }
+                __syncwarp();
+                if (FUSED_DQ) {
+                    if (gi > 0 && !(ok = warp_wait(&bars->dq_empty, (gi - 1) & 1, bars, status))) break;
+                    tc_fence_after_sync();
+                    if (leader) {
+#pragma unroll
+                        for (int ks = 0; ks < BN / 16; ++ks)
+                            mma_ss(tmem + C::COL_DQ, sdesc_advance(k_mn, ks * 2048),
+                                   sdesc_advance(ds_mn, dsoff + ks * 2048), idesc_dq, ks > 0 ? 1u : 0u);
+                        tc_commit(&bars->dq_full);
+                        tc_commit(&bars->ds_empty[b]);
+                    }
+                    __syncwarp();
+                }
             }
+            if (!ok) break;
+            if (leader) tc_commit(&bars->done);   // every MMA of this item (K, V, the accumulators)
             __syncwarp();
-            if (FUSED_DQ && nx < n) {   // next S^T: its columns are free once the dV MMA above has read P^T
-                if (!(ok = warp_wait(&bars->q_full[stn], (nx / NSQ) & 1, bars, status))) break;
-                tc_fence_after_sync();
-                if (leader) {
-                    issue_s<HD>(tmem + C::COL_S, tmem + C::COL_KT, sdesc_advance(q_km, stn * C::Q_BYTES), idesc_s);
-                    tc_commit(&bars->s_full[0]);
-                }
-                __syncwarp();
-            }
-            // dS^T is in TMEM (first columns of dP^T) and in smem: dK first (reads the TMEM copy),
-            // then the next dP^T may overwrite those columns
-            if (!(ok = warp_wait(&bars->ds_full[b], ph2, bars, status))) break;
-            tc_fence_after_sync();
-            if (leader) {
-#pragma unroll
-                for (int ks = 0; ks < BM / 16; ++ks)
-                    mma_ts(tmem + C::COL_DK, tmem + C::COL_DP + ks * 8, sdesc_advance(q_mn, qoff + ks * 2048), idesc_acc,
-                           (it > 0 || ks > 0) ? 1u : 0u);
-                tc_commit(&bars->q_empty[st]);
-                if (nx < n) {
-                    issue_rows_dot<HD>(tmem + C::COL_DP, v_km, sdesc_advance(do_km, stn * C::Q_BYTES));
-                    tc_commit(&bars->dp_full);
-                }
-            }
-            __syncwarp();
-            if (FUSED_DQ) {
-                if (it > 0 && !(ok = warp_wait(&bars->dq_empty, (it - 1) & 1, bars, status))) break;
-                tc_fence_after_sync();
-                if (leader) {
-#pragma unroll
-                    for (int ks = 0; ks < BN / 16; ++ks)
-                        mma_ss(tmem + C::COL_DQ, sdesc_advance(k_mn, ks * 2048), sdesc_advance(ds_mn, dsoff + ks * 2048),
-                               idesc_dq, ks > 0 ? 1u : 0u);
-                    tc_commit(&bars->dq_full);
-                    tc_commit(&bars->ds_empty[b]);
-                }
-                __syncwarp();
-            }
+            gt += n;
         }
         if (leader) {
-            if (ok) tc_commit(&bars->done);
             tc_commit(&bars->drain);
             mbar_wait(&bars->drain, 0, nullptr);
         }
         __syncwarp();
     } else if (warp < 4) {
-        // thread = key row r of this CTA (TMEM lane)
+        // thread = key row r of the item's key tile (TMEM lane)
         const int r = warp * 32 + lane;
-        const int key = j0 + r;
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        // K_j row r -> TMEM (bf16 pairs along hd) as the A operand of S^T = K_j Q_i^T
-        bool ok = warp_wait(&bars->kv_full, 0, bars, status);
-        if (ok) {
+        uint32_t gt = 0;   // query tiles of earlier items
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const int item = take_item(bars, k, status, ok);
+            if (item < 0) break;
+            const Item w = item_of(item);
+            const int head = w.head, j0 = w.j0, it0 = w.it0, n = w.n;
+            const int key = j0 + r;
+            // K_j row r -> TMEM (bf16 pairs along hd) as the A operand of S^T = K_j Q_i^T; the previous
+            // item's S^T MMAs, which read these columns, are done (this warp has waited for them below)
+            if ((ok = warp_wait(&bars->kv_full, k & 1, bars, status))) {
 #pragma unroll
-            for (int sub = 0; sub < C::SUB; ++sub) {
-                uint32_t kw[32];
-                const uint8_t *krow = smem + C::OFF_K + sub * C::KV_SUB + r * 128;
+                for (int sub = 0; sub < C::SUB; ++sub) {
+                    uint32_t kw[32];
+                    const uint8_t *krow = smem + C::OFF_K + sub * C::KV_SUB + r * 128;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 v4 = *reinterpret_cast<const uint4 *>(krow + ((c ^ (r & 7)) << 4));
-                    kw[4 * c + 0] = v4.x;
-                    kw[4 * c + 1] = v4.y;
-                    kw[4 * c + 2] = v4.z;
-                    kw[4 * c + 3] = v4.w;
-                }
-                tmem_st32(tmem + lane_off + C::COL_KT + 32 * sub, kw);
-            }
-            tmem_wait_st();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->kt_full);
-        }
-        for (int it = 0; ok && it < n; ++it) {
-            const int b = it & 1, st = it % NSQ;
-            const uint32_t ph2 = (it >> 1) & 1;
-            const int i0 = (it0 + it) * BM;
-            const float *Ls = ld_s + st * 2 * BM;
-            const float *Ds = Ls + BM;
-            // S^T of this tile: one buffer (phase per tile) or two alternating (phase per pair)
-            const uint32_t t_s = tmem + lane_off + C::col_s(!FUSED_DQ, it);
-            if (!(ok = FUSED_DQ ? warp_wait(&bars->s_full[0], it & 1, bars, status)
-                                : warp_wait(&bars->s_full[b], ph2, bars, status)))
-                break;
-            tc_fence_after_sync();
-            uint32_t sr[64];
-            tmem_ld32(t_s, sr);
-            tmem_ld32(t_s + 32, sr + 32);
-            tmem_wait_ld();
-            reg_fence32(sr);
-            reg_fence32(sr + 32);
-            // p = 2^(s * scale * log2(e) - L * log2(e)) on packed pairs; -L*log2(e) comes from the pre-pass
-            const uint64_t cs2 = f2_pack(scale_log2, scale_log2);
-            const bool diag = key > i0;   // some (key > row) pairs in this tile
-            uint64_t pp[32];              // P pairs (fp32) kept for dS
-            // dropout: element (row i0 + c, key) has flat index (head*S + i0 + c)*S + key; its index times
-            // the golden ratio steps by S * golden per column.  Keep bits of the 64 columns in km.
-            uint32_t km[2] = {0u, 0u};
-            uint64_t drop_g = DROP ? (((uint64_t)head * S + (uint64_t)i0) * (uint64_t)S + (uint64_t)key) * kDropGolden
-                                   : 0ull;
-            const uint64_t drop_step = DROP ? (uint64_t)S * kDropGolden : 0ull;
-            {
-                uint32_t pk[32];
-#pragma unroll
-                for (int c = 0; c < 64; c += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4 *>(Ls + c);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int cc = c + 2 * h;
-                        const float2 a = f2_unpack(ffma2(f2_pack(__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])), cs2,
-                                                         h == 0 ? f2_pack(l4.x, l4.y) : f2_pack(l4.z, l4.w)));
-                        float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
-                        if (diag) {
-                            if (key > i0 + cc) p0 = 0.0f;
-                            if (key > i0 + cc + 1) p1 = 0.0f;
-                        }
-                        pp[cc / 2] = f2_pack(p0, p1);
-                        if (DROP) {
-                            const bool k0 = drop_keep(drop.seed, drop_g, drop.keep_thr);
-                            const bool k1 = drop_keep(drop.seed, drop_g + drop_step, drop.keep_thr);
-                            drop_g += 2 * drop_step;
-                            km[cc / 32] |= ((uint32_t)k0 << (cc % 32)) | ((uint32_t)k1 << (cc % 32 + 1));
-                            pk[cc / 2] = pack_bf16x2(k0 ? p0 * drop.inv_keep : 0.0f, k1 ? p1 * drop.inv_keep : 0.0f);
-                        } else {
-                            pk[cc / 2] = pack_bf16x2(p0, p1);
-                        }
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 v4 = *reinterpret_cast<const uint4 *>(krow + ((c ^ (r & 7)) << 4));
+                        kw[4 * c + 0] = v4.x;
+                        kw[4 * c + 1] = v4.y;
+                        kw[4 * c + 2] = v4.z;
+                        kw[4 * c + 3] = v4.w;
                     }
+                    tmem_st32(tmem + lane_off + C::COL_KT + 32 * sub, kw);
                 }
-                tmem_st32(t_s, pk);
                 tmem_wait_st();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->kt_full);
             }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->p_full);
-
-            if (!(ok = warp_wait(&bars->dp_full, it & 1, bars, status))) break;
-            tc_fence_after_sync();
-            if (FUSED_DQ && it >= 2 && !(ok = warp_wait(&bars->ds_empty[b], ph2 ^ 1, bars, status))) break;
-            uint8_t *dsrow = smem + C::OFF_DS + b * C::DS_BYTES + r * 128;
-            // dS = P (dP - D) scale on packed pairs
-            const uint64_t sc2 = f2_pack(scale, scale);
-            const uint64_t m1 = f2_pack(-1.0f, -1.0f);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t dp[32];
-                tmem_ld32(tmem + lane_off + C::COL_DP + 32 * h, dp);
+            for (int it = 0; ok && it < n; ++it) {
+                const uint32_t gi = gt + it;
+                const int b = gi & 1, st = gi % NSQ;
+                const uint32_t ph2 = (gi >> 1) & 1;
+                const int i0 = (it0 + it) * BM;
+                const float *Ls = ld_s + st * 2 * BM;
+                const float *Ds = Ls + BM;
+                // S^T of this tile: one buffer (phase per tile) or two alternating (phase per pair)
+                const uint32_t t_s = tmem + lane_off + C::col_s(!FUSED_DQ, gi);
+                if (!(ok = FUSED_DQ ? warp_wait(&bars->s_full[0], gi & 1, bars, status)
+                                    : warp_wait(&bars->s_full[b], ph2, bars, status)))
+                    break;
+                tc_fence_after_sync();
+                uint32_t sr[64];
+                tmem_ld32(t_s, sr);
+                tmem_ld32(t_s + 32, sr + 32);
                 tmem_wait_ld();
-                reg_fence32(dp);
-                uint32_t pk[16];
+                reg_fence32(sr);
+                reg_fence32(sr + 32);
+                // p = 2^(s * scale * log2(e) - L * log2(e)) on packed pairs; -L*log2(e) comes from the pre-pass
+                const uint64_t cs2 = f2_pack(scale_log2, scale_log2);
+                const bool diag = key > i0;   // some (key > row) pairs in this tile
+                uint64_t pp[32];              // P pairs (fp32) kept for dS
+                // dropout: element (row i0 + c, key) has flat index (head*S + i0 + c)*S + key; its index times
+                // the golden ratio steps by S * golden per column.  Keep bits of the 64 columns in km.
+                uint32_t km[2] = {0u, 0u};
+                uint64_t drop_g = DROP ? (((uint64_t)head * S + (uint64_t)i0) * (uint64_t)S + (uint64_t)key) * kDropGolden
+                                       : 0ull;
+                const uint64_t drop_step = DROP ? (uint64_t)S * kDropGolden : 0ull;
+                {
+                    uint32_t pk[32];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int c = 32 * h + 2 * e;
-                    const float2 d2 = *reinterpret_cast<const float2 *>(Ds + c);
-                    float dp0 = __uint_as_float(dp[2 * e]), dp1 = __uint_as_float(dp[2 * e + 1]);
-                    if (DROP) {   // the dropout node's backward: dP = C o (dO V^T)
-                        dp0 = (km[c / 32] >> (c % 32)) & 1u ? dp0 * drop.inv_keep : 0.0f;
-                        dp1 = (km[c / 32] >> (c % 32 + 1)) & 1u ? dp1 * drop.inv_keep : 0.0f;
-                    }
-                    const uint64_t t = ffma2(f2_pack(d2.x, d2.y), m1, f2_pack(dp0, dp1));
-                    const float2 ds = f2_unpack(fmul2(fmul2(pp[c / 2], sc2), t));
-                    pk[e] = pack_bf16x2(ds.x, ds.y);
-                }
-                // dS^T pairs into the dP^T columns already read (A operand of dK += dS^T Q_i)
-                tmem_st16(tmem + lane_off + C::COL_DP + 16 * h, pk);
-                if (FUSED_DQ) {
+                    for (int c = 0; c < 64; c += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4 *>(Ls + c);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const int chunk = 4 * h + v;                   // 16-byte chunk of the 128-byte row
-                        uint4 w;
-                        w.x = pk[4 * v + 0];
-                        w.y = pk[4 * v + 1];
-                        w.z = pk[4 * v + 2];
-                        w.w = pk[4 * v + 3];
-                        *reinterpret_cast<uint4 *>(dsrow + ((chunk ^ (r & 7)) << 4)) = w;
+                        for (int h = 0; h < 2; ++h) {
+                            const int cc = c + 2 * h;
+                            const float2 a = f2_unpack(ffma2(f2_pack(__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])), cs2,
+                                                             h == 0 ? f2_pack(l4.x, l4.y) : f2_pack(l4.z, l4.w)));
+                            float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
+                            if (diag) {
+                                if (key > i0 + cc) p0 = 0.0f;
+                                if (key > i0 + cc + 1) p1 = 0.0f;
+                            }
+                            pp[cc / 2] = f2_pack(p0, p1);
+                            if (DROP) {
+                                const bool k0 = drop_keep(drop.seed, drop_g, drop.keep_thr);
+                                const bool k1 = drop_keep(drop.seed, drop_g + drop_step, drop.keep_thr);
+                                drop_g += 2 * drop_step;
+                                km[cc / 32] |= ((uint32_t)k0 << (cc % 32)) | ((uint32_t)k1 << (cc % 32 + 1));
+                                pk[cc / 2] = pack_bf16x2(k0 ? p0 * drop.inv_keep : 0.0f, k1 ? p1 * drop.inv_keep : 0.0f);
+                            } else {
+                                pk[cc / 2] = pack_bf16x2(p0, p1);
+                            }
+                        }
+                    }
+                    tmem_st32(t_s, pk);
+                    tmem_wait_st();
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->p_full);
+
+                if (!(ok = warp_wait(&bars->dp_full, gi & 1, bars, status))) break;
+                tc_fence_after_sync();
+                if (FUSED_DQ && gi >= 2 && !(ok = warp_wait(&bars->ds_empty[b], ph2 ^ 1, bars, status))) break;
+                uint8_t *dsrow = smem + C::OFF_DS + b * C::DS_BYTES + r * 128;
+                // dS = P (dP - D) scale on packed pairs
+                const uint64_t sc2 = f2_pack(scale, scale);
+                const uint64_t m1 = f2_pack(-1.0f, -1.0f);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t dp[32];
+                    tmem_ld32(tmem + lane_off + C::COL_DP + 32 * h, dp);
+                    tmem_wait_ld();
+                    reg_fence32(dp);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int c = 32 * h + 2 * e;
+                        const float2 d2 = *reinterpret_cast<const float2 *>(Ds + c);
+                        float dp0 = __uint_as_float(dp[2 * e]), dp1 = __uint_as_float(dp[2 * e + 1]);
+                        if (DROP) {   // the dropout node's backward: dP = C o (dO V^T)
+                            dp0 = (km[c / 32] >> (c % 32)) & 1u ? dp0 * drop.inv_keep : 0.0f;
+                            dp1 = (km[c / 32] >> (c % 32 + 1)) & 1u ? dp1 * drop.inv_keep : 0.0f;
+                        }
+                        const uint64_t t = ffma2(f2_pack(d2.x, d2.y), m1, f2_pack(dp0, dp1));
+                        const float2 ds = f2_unpack(fmul2(fmul2(pp[c / 2], sc2), t));
+                        pk[e] = pack_bf16x2(ds.x, ds.y);
+                    }
+                    // dS^T pairs into the dP^T columns already read (A operand of dK += dS^T Q_i)
+                    tmem_st16(tmem + lane_off + C::COL_DP + 16 * h, pk);
+                    if (FUSED_DQ) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int chunk = 4 * h + v;                   // 16-byte chunk of the 128-byte row
+                            uint4 w;
+                            w.x = pk[4 * v + 0];
+                            w.y = pk[4 * v + 1];
+                            w.z = pk[4 * v + 2];
+                            w.w = pk[4 * v + 3];
+                            *reinterpret_cast<uint4 *>(dsrow + ((chunk ^ (r & 7)) << 4)) = w;
+                        }
                     }
                 }
+                tmem_wait_st();
+                if (FUSED_DQ) fence_proxy_async_smem();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->ds_full[b]);
             }
-            tmem_wait_st();
-            if (FUSED_DQ) fence_proxy_async_smem();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->ds_full[b]);
-        }
-        // epilogue: dV rows, staged in the query-tile ring (free once every MMA has completed);
-        // the four warps decide together, since the staging ends in a barrier of all 128 threads
-        if (named_bar_and(2, 128, ok && warp_wait(&bars->done, 0, bars, status))) {
+            if (!ok) break;
+            // epilogue: dV rows straight from TMEM to global memory once every MMA of the item is done
+            if (!(ok = warp_wait(&bars->done, k & 1, bars, status))) break;
             tc_fence_after_sync();
-            store_rows_tma<HD>(tmem + lane_off + C::COL_DV, smem + C::OFF_Q, r, &tm_dv, j0, head, 2, threadIdx.x == 0);
+            store_rows_global<HD>(tmem + lane_off + C::COL_DV, dV + ((size_t)head * S + min(key, S - 1)) * HD, key < S);
+            gt += n;
         }
     } else if (warp < 8) {
-        // dQ readout: thread = hd index d (TMEM lane of dQ^T)
+        // dQ readout: thread = hd index d (TMEM lane of dQ^T); then the item's dK rows (thread = key)
         const int wq = warp - 4;
         const int d = wq * 32 + lane;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        uint32_t gt = 0;   // query tiles of earlier items
         bool ok = true;
-        if (FUSED_DQ && d < HD) {
-            for (int it = 0; it < n; ++it) {
-                // the readout warps stay in step: all leave the loop together if one gives up
-                if (!(ok = named_bar_and(1, HD, warp_wait(&bars->dq_full, it & 1, bars, status)))) break;
-                tc_fence_after_sync();
-                uint32_t g[64];
-                tmem_ld32(tmem + lane_off + C::COL_DQ, g);
-                tmem_ld32(tmem + lane_off + C::COL_DQ + 32, g + 32);
-                tmem_wait_ld();
-                reg_fence32(g);
-                reg_fence32(g + 32);
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->dq_empty);
-                const int i0 = (it0 + it) * BM;
-                const int rows = min(BM, S - i0);
-                // the staging tile is free once the previous bulk reduce has read it
-                if (d == 0) bulk_wait_group_read0();
-                named_bar_sync(1, HD);
+        for (int k = 0; ok; ++k) {
+            const int item = take_item(bars, k, status, ok);
+            if (item < 0) break;
+            const Item w = item_of(item);
+            if (FUSED_DQ && d < HD) {
+                for (int it = 0; it < w.n; ++it) {
+                    const uint32_t gi = gt + it;
+                    // the readout warps stay in step: all leave the loop together if one gives up
+                    if (!(ok = named_bar_and(1, HD, warp_wait(&bars->dq_full, gi & 1, bars, status)))) break;
+                    tc_fence_after_sync();
+                    uint32_t g[64];
+                    tmem_ld32(tmem + lane_off + C::COL_DQ, g);
+                    tmem_ld32(tmem + lane_off + C::COL_DQ + 32, g + 32);
+                    tmem_wait_ld();
+                    reg_fence32(g);
+                    reg_fence32(g + 32);
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->dq_empty);
+                    const int i0 = (w.it0 + it) * BM;
+                    const int rows = min(BM, S - i0);
+                    // the staging tile is free once the previous bulk reduce has read it
+                    if (d == 0) bulk_wait_group_read0();
+                    named_bar_sync(1, HD);
 #pragma unroll
-                for (int c = 0; c < BM; ++c) dq_stage[c * HD + d] = __uint_as_float(g[c]);
-                fence_proxy_async_smem();
-                named_bar_sync(1, HD);
-                if (d == 0) {
-                    bulk_reduce_add_f32(dq_acc + ((size_t)head * S + i0) * HD, dq_stage, (uint32_t)(rows * HD * 4));
-                    bulk_commit_group();
+                    for (int c = 0; c < BM; ++c) dq_stage[c * HD + d] = __uint_as_float(g[c]);
+                    fence_proxy_async_smem();
+                    named_bar_sync(1, HD);
+                    if (d == 0) {
+                        bulk_reduce_add_f32(dq_acc + ((size_t)w.head * S + i0) * HD, dq_stage,
+                                            (uint32_t)(rows * HD * 4));
+                        bulk_commit_group();
+                    }
                 }
             }
-            if (d == 0) bulk_wait_group_read0();   // the staging tile is read; the adds complete before the grid does
-        }
-        // epilogue: dK rows (same TMEM lanes as warps 0-3: thread = key), staged in the dO ring;
-        // decided together by the four warps, as for dV
-        if (named_bar_and(3, 128, ok && warp_wait(&bars->done, 0, bars, status))) {
+            if (!ok) break;
+            // dK rows (same TMEM lanes as warps 0-3: thread = key) once every MMA of the item is
+            // done; then the next item's first dK MMA may overwrite the accumulator
+            if (!(ok = warp_wait(&bars->done, k & 1, bars, status))) break;
             tc_fence_after_sync();
-            store_rows_tma<HD>(tmem + lane_off + C::COL_DK, smem + C::OFF_DO, wq * 32 + lane, &tm_dk, j0, head, 3,
-                               wq == 0 && lane == 0);
+            const int key = w.j0 + wq * 32 + lane;
+            store_rows_global<HD>(tmem + lane_off + C::COL_DK, dK + ((size_t)w.head * S + min(key, S - 1)) * HD,
+                                  key < S);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->dk_read);
+            gt += w.n;
         }
+        if (FUSED_DQ && d == 0) bulk_wait_group_read0();   // the staging tile is read; the adds complete before the grid does
     }
 
     tc_fence_before_sync();
@@ -571,28 +654,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Work-item counters of the persistent key-tile kernel: one slot per launch, handed out
+// round-robin so that launches in flight on different streams use different slots, and zeroed
+// on the launch's stream just before it (a memset node when the launch is captured in a graph).
+constexpr int kSchedSlots = 64;
+__device__ unsigned g_next_item[kSchedSlots];
+std::atomic<unsigned> g_next_slot{0};
+
+int next_item_counter(cudaStream_t st, unsigned **ctr)
+{
+    void *base = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&base, g_next_item);
+    if (e != cudaSuccess) return XFA_ERR_CUDA_BASE + (int)e;
+    *ctr = static_cast<unsigned *>(base) + g_next_slot.fetch_add(1u) % kSchedSlots;
+    e = cudaMemsetAsync(*ctr, 0, sizeof(unsigned), st);
+    return e == cudaSuccess ? XFA_OK : XFA_ERR_CUDA_BASE + (int)e;
+}
+
 template <int HD, bool FUSED_DQ, bool DROP>
 int run(const BwdParams &p, cudaStream_t st)
 {
-    alignas(64) CUtensorMap tk, tv, tq, tdo, tdk, tdv;
+    alignas(64) CUtensorMap tk, tv, tq, tdo;
     int rc = encode_tmap_bf16_3d(&tk, p.k, HD, p.S, p.bh, BN);
     if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tv, p.v, HD, p.S, p.bh, BN);
     if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tq, p.q, HD, p.S, p.bh, BM);
     if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tdo, p.dout, HD, p.S, p.bh, BM);
-    if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tdk, p.dk, HD, p.S, p.bh, BN);
-    if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tdv, p.dv, HD, p.S, p.bh, BN);
     if (rc != XFA_OK) return rc;
     static_assert(Cfg<HD>::SMEM <= 227 * 1024, "shared memory per CTA");
-    static_assert(Cfg<HD>::NSQ * Cfg<HD>::Q_BYTES >= Cfg<HD>::KV_BYTES, "dK / dV staging fits a ring");
     auto kern = tc_bwd_kernel<HD, FUSED_DQ, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<HD>::SMEM);
     if (e != cudaSuccess) return XFA_ERR_CUDA_BASE + (int)e;
     const int nkt = (p.S + BN - 1) / BN;
-    const unsigned grid = (unsigned)(nkt * p.bh);
-    kern<<<grid, kThreads, Cfg<HD>::SMEM, st>>>(tk, tv, tq, tdo, tdk, tdv, p.Lg, p.D, p.dq_acc, (__nv_bfloat16 *)p.dk,
+    const unsigned grid = (unsigned)std::min(nkt * p.bh, device_sm_count());   // persistent: one CTA per SM
+    unsigned *ctr = nullptr;
+    if ((rc = next_item_counter(st, &ctr)) != XFA_OK) return rc;
+    kern<<<grid, kThreads, Cfg<HD>::SMEM, st>>>(tk, tv, tq, tdo, p.Lg, p.D, p.dq_acc, (__nv_bfloat16 *)p.dk,
                                                  (__nv_bfloat16 *)p.dv, p.bh, p.S, p.S_pad, p.scale,
                                                  p.scale * 1.4426950408889634f, p.status, p.drop,
-                                                 head_bundle(p.bh, p.S, HD, 2, kHeadBundle));
+                                                 head_bundle(p.bh, p.S, HD, 2, kHeadBundle), ctr);
     e = cudaGetLastError();
     return e == cudaSuccess ? XFA_OK : XFA_ERR_CUDA_BASE + (int)e;
 }
