@@ -483,27 +483,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before_sync();
     __syncthreads();
+    if (threadIdx.x == 0) {
+        // this CTA has claimed its last item; the last CTA out returns the counter slot to zero
+        __threadfence();
+        if (atomicAdd(next_item + 1, 1u) == gridDim.x - 1) {
+            next_item[0] = 0u;
+            next_item[1] = 0u;
+            __threadfence();
+        }
+    }
     if (warp == kWarpMma) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, 512);
     }
 }
 
-// Work-item counters of the persistent forward: one slot per launch, handed out round-robin so
-// that launches in flight on different streams use different slots, and zeroed on the launch's
-// stream just before it (a memset node when the launch is captured in a graph).
+// Work-item counters of the persistent forward: a slot per launch (two words: items claimed,
+// CTAs finished), handed out round-robin so that launches in flight on different streams use
+// different slots.  The last CTA of a launch to finish sets both words back to zero (every CTA
+// has claimed past the end of the list by then), so a slot is zero whenever a launch starts --
+// no memset on the stream, and graph replays reuse their slot.  Static memory starts at zero.
 constexpr int kSchedSlots = 64;
-__device__ unsigned g_next_item[kSchedSlots];
+__device__ unsigned g_next_item[2 * kSchedSlots];
 std::atomic<unsigned> g_next_slot{0};
 
-int next_item_counter(cudaStream_t st, unsigned **ctr)
+int next_item_counter(unsigned **ctr)
 {
     void *base = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&base, g_next_item);
+    const cudaError_t e = cudaGetSymbolAddress(&base, g_next_item);
     if (e != cudaSuccess) return XFA_ERR_CUDA_BASE + (int)e;
-    *ctr = static_cast<unsigned *>(base) + g_next_slot.fetch_add(1u) % kSchedSlots;
-    e = cudaMemsetAsync(*ctr, 0, sizeof(unsigned), st);
-    return e == cudaSuccess ? XFA_OK : XFA_ERR_CUDA_BASE + (int)e;
+    *ctr = static_cast<unsigned *>(base) + 2 * (g_next_slot.fetch_add(1u) % kSchedSlots);
+    return XFA_OK;
 }
 
 template <int HD, bool DROP>
@@ -521,7 +531,7 @@ int run(const FwdParams &p, cudaStream_t st)
     const int nqb = (p.S + 2 * BM - 1) / (2 * BM);
     const unsigned grid = (unsigned)std::min(nqb * p.bh, device_sm_count());   // persistent: one CTA per SM
     unsigned *ctr = nullptr;
-    if ((rc = next_item_counter(st, &ctr)) != XFA_OK) return rc;
+    if ((rc = next_item_counter(&ctr)) != XFA_OK) return rc;
     kern<<<grid, kThreads, Cfg<HD>::SMEM, st>>>(tq, tk, tv, (__nv_bfloat16 *)p.out, p.lse, p.bh, p.S,
                                                  p.scale * 1.4426950408889634f, p.status, p.drop,
                                                  head_bundle(p.bh, p.S, HD, 2, kHeadBundle), ctr);
