@@ -74,14 +74,17 @@ struct Cfg {
     // TMEM columns: dK, dV accumulators; S^T (P^T bf16 written back into its first 32 columns);
     // dP^T (dS^T bf16 written back into its first 32 columns); dQ^T; K_j as a bf16 A operand.
     static constexpr uint32_t COL_DK = 0, COL_DV = HD, COL_S = 2 * HD, COL_DP = 2 * HD + 64,
-                              COL_DQ = 2 * HD + 128, COL_KT = 2 * HD + 192;
-    // S^T buffer of query tile i: with the fused dQ one buffer; without it (the dQ^T
-    // columns are free) tiles alternate between COL_S and COL_DQ.
-    static __device__ __forceinline__ uint32_t col_s(bool two_buffers, int i)
-    {
-        return two_buffers && (i & 1) ? COL_DQ : COL_S;
-    }
+                              COL_DQ = 2 * HD + 128, COL_KT = 2 * HD + 192, COL_S2 = COL_KT + HD / 2;
     static constexpr uint32_t TMEM_COLS = 512;
+    // S^T buffers: query tiles alternate between two when there is room -- without the fused dQ
+    // (the dQ^T columns are free) or at hd = 64 (columns past K_j) -- else they share one.
+    template <bool FUSED_DQ>
+    static __host__ __device__ constexpr bool two_s() { return !FUSED_DQ || COL_S2 + 64 <= TMEM_COLS; }
+    template <bool FUSED_DQ>
+    static __device__ __forceinline__ uint32_t col_s(uint32_t i)
+    {
+        return two_s<FUSED_DQ>() && (i & 1) ? (FUSED_DQ ? COL_S2 : COL_DQ) : COL_S;
+    }
 };
 
 constexpr int kMaxRing = 4;
@@ -191,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     using C = Cfg<HD>;
     constexpr int NSQ = C::NSQ;
+    constexpr bool TWO_S = C::template two_s<FUSED_DQ>();
     static_assert(NSQ <= kMaxRing && sizeof(Bars) <= 256, "barrier block");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -343,9 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader) {
                 // the S^T / dP^T columns last held the previous item's final P^T / dS^T, read by
                 // its dV / dK MMAs issued before (in order)
-                issue_s<HD>(tmem + C::col_s(!FUSED_DQ, gt), tmem + C::COL_KT,
+                issue_s<HD>(tmem + C::template col_s<FUSED_DQ>(gt), tmem + C::COL_KT,
                             sdesc_advance(q_km, st0 * C::Q_BYTES), idesc_s);
-                tc_commit(&bars->s_full[FUSED_DQ ? 0 : (gt & 1)]);
+                tc_commit(&bars->s_full[TWO_S ? (gt & 1) : 0]);
                 issue_rows_dot<HD>(tmem + C::COL_DP, v_km, sdesc_advance(do_km, st0 * C::Q_BYTES));
                 tc_commit(&bars->dp_full);
             }
@@ -358,16 +362,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nx = it + 1;
                 const uint32_t gn = gi + 1;
                 const int stn = gn % NSQ;
-                // Next S^T.  Without the fused dQ it goes first, into the other S^T buffer, so that it
+                // Next S^T.  With two S^T buffers it goes first, into the other one, so that it
                 // does not queue behind this tile's work (that buffer's P^T, tile gi - 1, was read by
                 // the dV MMA issued one iteration ago, and the in-order pipe runs that MMA first).
                 // With one buffer it follows this tile's dV, which reads P^T from the same columns.
-                const bool s_first = !FUSED_DQ && nx < n;
+                const bool s_first = TWO_S && nx < n;
                 if (s_first) {
                     if (!(ok = warp_wait(&bars->q_full[stn], (gn / NSQ) & 1, bars, status))) break;
                     tc_fence_after_sync();
                     if (leader) {
-                        issue_s<HD>(tmem + C::col_s(true, gn), tmem + C::COL_KT, sdesc_advance(q_km, stn * C::Q_BYTES),
+                        issue_s<HD>(tmem + C::template col_s<FUSED_DQ>(gn), tmem + C::COL_KT, sdesc_advance(q_km, stn * C::Q_BYTES),
                                     idesc_s);
                         tc_commit(&bars->s_full[gn & 1]);
                     }
@@ -381,11 +385,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (leader) {
 #pragma unroll
                     for (int ks = 0; ks < BM / 16; ++ks)
-                        mma_ts(tmem + C::COL_DV, tmem + C::col_s(!FUSED_DQ, gi) + ks * 8,
+                        mma_ts(tmem + C::COL_DV, tmem + C::template col_s<FUSED_DQ>(gi) + ks * 8,
                                sdesc_advance(do_mn, qoff + ks * 2048), idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
                 }
                 __syncwarp();
-                if (FUSED_DQ && nx < n) {   // next S^T: its columns are free once the dV MMA above has read P^T
+                if (!TWO_S && nx < n) {   // next S^T: its columns are free once the dV MMA above has read P^T
                     if (!(ok = warp_wait(&bars->q_full[stn], (gn / NSQ) & 1, bars, status))) break;
                     tc_fence_after_sync();
                     if (leader) {
@@ -478,8 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float *Ls = ld_s + st * 2 * BM;
                 const float *Ds = Ls + BM;
                 // S^T of this tile: one buffer (phase per tile) or two alternating (phase per pair)
-                const uint32_t t_s = tmem + lane_off + C::col_s(!FUSED_DQ, gi);
-                if (!(ok = FUSED_DQ ? warp_wait(&bars->s_full[0], gi & 1, bars, status)
+                const uint32_t t_s = tmem + lane_off + C::template col_s<FUSED_DQ>(gi);
+                if (!(ok = !TWO_S ? warp_wait(&bars->s_full[0], gi & 1, bars, status)
                                     : warp_wait(&bars->s_full[b], ph2, bars, status)))
                     break;
                 tc_fence_after_sync();

@@ -65,3 +65,35 @@ def test_graph_replay_matches_eager(dtype, hd, impl, exact):
             else:   # dQ summed with atomics in a data-dependent order (bf16: one rounding step apart)
                 tol = (1e-2 if dtype == "bf16" else 1e-5) * float(a.float().abs().max())
                 assert torch.allclose(a.float(), b.float(), rtol=0, atol=tol)
+
+
+def test_concurrent_streams_and_counter_reuse():
+    """The persistent tensor-core kernels take work items from a per-launch counter slot.  Forward
+    and backward launches in flight on four streams at once, and more launches than there are
+    slots (each slot resets itself when its launch ends), give the results of a lone launch."""
+    from bwd_xfa_fwd_gb300 import binding
+    bh, S, hd = 4, 1000, 128
+    scale = 1.0 / math.sqrt(hd)
+    cases = []
+    for i in range(4):
+        x = inputs.draw((bh, S, hd), "bf16", seed=300 + i)
+        q, k, v, do = (to_device(x[n], "bf16") for n in ("q", "k", "v", "dout"))
+        out, lse = binding.fwd(q, k, v, scale, binding.IMPL_TCGEN05_DET)
+        grads = binding.bwd(q, k, v, out, do, lse, scale, binding.IMPL_TCGEN05_DET)
+        torch.cuda.synchronize()
+        cases.append(dict(qkvd=(q, k, v, do), ref=[t.clone() for t in (out, lse) + tuple(grads)]))
+    streams = [torch.cuda.Stream() for _ in cases]
+    for rep in range(20):   # 20 x 4 x 2 persistent launches: every counter slot is reused
+        outs = []
+        for c, st in zip(cases, streams):
+            st.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(st):
+                q, k, v, do = c["qkvd"]
+                out, lse = binding.fwd(q, k, v, scale, binding.IMPL_TCGEN05_DET)
+                grads = binding.bwd(q, k, v, out, do, lse, scale, binding.IMPL_TCGEN05_DET)
+                outs.append((out, lse) + tuple(grads))
+        torch.cuda.synchronize()
+        assert binding.status() == binding.XFA_OK
+        for c, o in zip(cases, outs):
+            for a, b in zip(c["ref"], o):
+                assert torch.equal(a, b), f"repetition {rep}"
