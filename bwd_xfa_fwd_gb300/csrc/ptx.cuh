@@ -101,17 +101,6 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
-// 3-D tiled bulk tensor store shared -> global, tracked by the issuing thread's bulk
-// async-group.  The box is the map's box; rows past the tensor's extent are not written.
-// Coordinates as for tma_load_3d (x * elt 16-byte aligned, none negative).
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y, int z)
-{
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-
 // Plain bulk copy global -> shared (16-byte aligned addresses, size multiple of 16).
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
 {
