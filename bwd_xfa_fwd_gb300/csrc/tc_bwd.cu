@@ -7,9 +7,10 @@
 //
 // GB300 design: the key-block-owned backward that the page names as its
 // follow-up, on tcgen05:
-//   * a CTA owns 128 keys of one head; K_j and V_j are loaded once by TMA and
-//     dK_j, dV_j accumulate in TMEM (128 lanes = keys, hd fp32 columns each)
-//     over every 64-row query tile at or below the diagonal;
+//   * persistent CTAs, one per SM; a work item is 128 keys of one head (claimed from a
+//     per-launch counter); K_j and V_j are loaded once per item by TMA and dK_j, dV_j
+//     accumulate in TMEM (128 lanes = keys, hd fp32 columns each) over every 64-row
+//     query tile at or below the diagonal, then go straight to global memory;
 //   * warp 8 streams Q_i, dO_i (TMA, 128-byte swizzle) with -L_i*log2(e) and
 //     D_i (bulk copies) through a ring;
 //   * warp 9 (one thread) issues, per query tile:
@@ -30,8 +31,9 @@
 // For hd = 64 the dQ^T MMA still runs with M = 128; lanes 64-127 hold
 // products of V and are never read.
 // Without the fused dQ (the deterministic variant) the dQ^T columns hold a second
-// S^T buffer: tiles alternate between the two, and S^T of the next tile is issued
-// before this tile's dV, so the key warps do not wait for it.
+// S^T buffer, and at hd = 64 the columns past K_j do: tiles alternate between the
+// two, and S^T of the next tile is issued before this tile's dV, so the key warps
+// do not wait for it.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 

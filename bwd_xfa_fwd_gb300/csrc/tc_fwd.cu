@@ -7,9 +7,10 @@
 // above the diagonal are never touched.
 //
 // GB300 design (replaces the page's one-block-per-row SIMT kernel):
-//   * a CTA owns 256 query rows of one head as two 128-row tiles (t = 0, 1);
-//   * warp 8 streams K and V tiles (128 keys x hd) through a TMA ring with
-//     128-byte swizzle; Q tiles are loaded once;
+//   * persistent CTAs, one per SM; a work item is 256 query rows of one head as two
+//     128-row tiles (t = 0, 1), claimed from a per-launch counter (see the kernel);
+//   * warp 8 claims items and streams Q and the K and V tiles (128 keys x hd) through
+//     a TMA ring with 128-byte swizzle; the ring runs on across items;
 //   * warp 9 (one thread) issues tcgen05.mma: S_t = Q_t K^T into TMEM
 //     (128 lanes x 128 fp32 columns) and O_t += P_t V with P_t read straight
 //     from TMEM (bf16, packed into the first 64 columns of S_t);
