@@ -131,9 +131,9 @@ SIMT_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # the SIMT kernels' arithmetic
 
 def workload_config(w):
     elt = 2 if w.dtype == "bf16" else 4
-    one = w.bh * w.S * w.hd * elt
-    l2 = (f"inputs (4 x {one / 2**20:.0f} MiB {w.dtype}) larger than L2 (129 MB); no flush" if one > L2_BYTES else
-          f"inputs (4 x {one / 2**20:.2f} MiB {w.dtype}) fit in L2 (129 MB): timed warm, a profiling case")
+    one = w.bh * w.S * w.hd * elt   # Q, K, V and dO, each streamed every step
+    l2 = (f"inputs (4 x {one / 2**20:.0f} MiB {w.dtype}) larger than L2 (129 MB); no flush" if 4 * one > L2_BYTES
+          else f"inputs (4 x {one / 2**20:.2f} MiB {w.dtype}) fit in L2 (129 MB): timed warm, a profiling case")
     return {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "hd": w.hd, "dtype": w.dtype,
             "scale": w.scale, "causal": True, "layout": "[bh,S,hd] row-major", "l2": l2}
 
