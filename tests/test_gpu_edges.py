@@ -28,7 +28,7 @@ def built():
 # "falling": it never moves after the first key.  "flat": uniform rows.
 @pytest.mark.parametrize("pattern", inputs.PATTERNS)
 @pytest.mark.parametrize("dtype,hd,impl", [("bf16", 128, 2), ("bf16", 64, 2), ("bf16", 128, 3), ("bf16", 64, 1),
-                                           ("f32", 64, 1), ("f32", 128, 1)])
+                                           ("f32", 64, 1), ("f32", 128, 1), ("f32", 64, 2), ("f32", 32, 2)])
 def test_running_max_patterns(pattern, dtype, hd, impl):
     bh, S = 2, 1000
     scale = 1.0 / math.sqrt(hd)
