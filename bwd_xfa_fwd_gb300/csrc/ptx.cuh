@@ -71,8 +71,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may stay suspended in the instruction until the phase
+// completes or `hint_ns` has passed (the suspend-time hint), instead of the system's shorter
+// default -- fewer polls of the barrier word in shared memory.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with parity `parity` of `bar` to complete.  Gives up
-// after `limit_ns` or as soon as `*abort` becomes nonzero; returns false then.
+// after `limit_ns` or as soon as `*abort` becomes nonzero; returns false then
+// (both checked every 4 suspended tries of at most 50 us each).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort,
                                           uint64_t limit_ns = kWaitLimitNs)
 {
@@ -81,8 +98,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
     const uint64_t t0 = globaltimer_ns();
     while (true) {
 #pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(a, parity)) return true;
+        for (int i = 0; i < 4; ++i)
+            if (mbar_try_wait_hint(a, parity, 50000u)) return true;
         if (abort && *abort) return false;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
