@@ -89,7 +89,9 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity
 
 // Wait for the phase with parity `parity` of `bar` to complete.  Gives up
 // after `limit_ns` or as soon as `*abort` becomes nonzero; returns false then
-// (both checked every 4 suspended tries of at most 50 us each).
+// (both checked every 4 suspended tries of at most 50 us each).  The waiting
+// thread sleeps; mbar_wait_spin below keeps polling instead (it sees the phase
+// complete sooner but takes more from the warps that work meanwhile).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort,
                                           uint64_t limit_ns = kWaitLimitNs)
 {
@@ -100,6 +102,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
 #pragma unroll 1
         for (int i = 0; i < 4; ++i)
             if (mbar_try_wait_hint(a, parity, 50000u)) return true;
+        if (abort && *abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// As mbar_wait, polling without a suspend-time hint.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, const volatile int *abort,
+                                               uint64_t limit_ns = kWaitLimitNs)
+{
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(a, parity)) return true;
         if (abort && *abort) return false;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }

@@ -64,7 +64,7 @@ __device__ __forceinline__ void fail(Bars *b, int *status)
 
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, Bars *b, int *status)
 {
-    bool ok = mbar_wait(bar, parity, &b->abort);
+    bool ok = mbar_wait_spin(bar, parity, &b->abort);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok && (threadIdx.x & 31) == 0) fail(b, status);
     return ok;
@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued[3] = {0, 0, 0};
             for (int j = 0; j < nkv; ++j) {
                 const int st = j % C::NS;
-                if (j >= C::NS && !mbar_wait(&bars->kv_empty[st], ((j / C::NS) + 1) & 1, &bars->abort)) {
+                if (j >= C::NS && !mbar_wait_spin(&bars->kv_empty[st], ((j / C::NS) + 1) & 1, &bars->abort)) {
                     fail(bars, status);
                     break;
                 }
@@ -160,12 +160,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issued[st] = j + 1;
             }
             // never leave the CTA with copies in flight
-            mbar_wait(&bars->qdo_full, 0, nullptr);
+            mbar_wait_spin(&bars->qdo_full, 0, nullptr);
             for (int st = 0; st < C::NS; ++st) {
                 if (issued[st] == 0) continue;
                 const uint32_t ph = ((issued[st] - 1) / C::NS) & 1;
-                mbar_wait(&bars->k_full[st], ph, nullptr);
-                mbar_wait(&bars->v_full[st], ph, nullptr);
+                mbar_wait_spin(&bars->k_full[st], ph, nullptr);
+                mbar_wait_spin(&bars->v_full[st], ph, nullptr);
             }
         }
     } else if (warp == kWarpMma) {
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) {
             if (ok) tc_commit(&bars->done);
             tc_commit(&bars->drain);
-            mbar_wait(&bars->drain, 0, nullptr);
+            mbar_wait_spin(&bars->drain, 0, nullptr);
         }
         __syncwarp();
     } else {

@@ -87,7 +87,7 @@ __device__ __forceinline__ void fail(Bars *b, int *status)
 // tcgen05 instructions after it are never reached by part of a warp.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, Bars *b, int *status)
 {
-    bool ok = mbar_wait(bar, parity, &b->abort);
+    bool ok = mbar_wait_spin(bar, parity, &b->abort);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok && (threadIdx.x & 31) == 0) fail(b, status);
     return ok;
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int kc = 0; ok; ++kc) {          // kc: items claimed, posted in ring entry kc & 1
                 const int e = kc & 1;
-                if (kc >= 2 && !(ok = mbar_wait(&bars->item_empty[e], ((kc >> 1) + 1) & 1, &bars->abort))) break;
+                if (kc >= 2 && !(ok = mbar_wait_spin(&bars->item_empty[e], ((kc >> 1) + 1) & 1, &bars->abort))) break;
                 int item = (int)atomicAdd(next_item, 1u);
                 if (item >= n_items) item = -1;
                 *reinterpret_cast<volatile int *>(&bars->item_id[e]) = item;
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool t1 = q0 + BM < S;
                 const int nkv = t1 ? 2 * qb + 2 : 2 * qb + 1;
                 // the Q buffers are free once the previous item's last S MMAs have read them
-                if (k > 0 && !(ok = mbar_wait(&bars->q_empty, (k - 1) & 1, &bars->abort))) break;
+                if (k > 0 && !(ok = mbar_wait_spin(&bars->q_empty, (k - 1) & 1, &bars->abort))) break;
                 mbar_arrive_expect_tx(&bars->q_full, (t1 ? 2 : 1) * C::TILE_BYTES);
                 for (int s = 0; s < C::SUB; ++s) {
                     tma_load_3d(smem + C::OFF_Q0 + s * C::SUB_BYTES, &tm_q, &bars->q_full, s * 64, q0, head);
@@ -242,13 +242,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < nkv; ++j, ++g) {
                     const int st = g % C::NS;
                     const uint32_t ph = ((g / C::NS) + 1) & 1;   // parity of the release of the previous use
-                    if (g >= C::NS && !(ok = mbar_wait(&bars->k_empty[st], ph, &bars->abort))) break;
+                    if (g >= C::NS && !(ok = mbar_wait_spin(&bars->k_empty[st], ph, &bars->abort))) break;
                     mbar_arrive_expect_tx(&bars->k_full[st], C::TILE_BYTES);
                     for (int s = 0; s < C::SUB; ++s)
                         tma_load_3d(smem + C::OFF_K + st * C::TILE_BYTES + s * C::SUB_BYTES, &tm_k, &bars->k_full[st],
                                     s * 64, j * BN, head);
                     last_k[st] = g + 1;
-                    if (g >= C::NS && !(ok = mbar_wait(&bars->v_empty[st], ph, &bars->abort))) break;
+                    if (g >= C::NS && !(ok = mbar_wait_spin(&bars->v_empty[st], ph, &bars->abort))) break;
                     mbar_arrive_expect_tx(&bars->v_full[st], C::TILE_BYTES);
                     for (int s = 0; s < C::SUB; ++s)
                         tma_load_3d(smem + C::OFF_V + st * C::TILE_BYTES + s * C::SUB_BYTES, &tm_v, &bars->v_full[st],
@@ -258,10 +258,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) fail(bars, status);
             // Never leave the CTA with copies in flight: wait for the last load of Q and of each stage.
-            if (k > 0) mbar_wait(&bars->q_full, (k - 1) & 1, nullptr);
+            if (k > 0) mbar_wait_spin(&bars->q_full, (k - 1) & 1, nullptr);
             for (int st = 0; st < C::NS; ++st) {
-                if (last_k[st]) mbar_wait(&bars->k_full[st], ((last_k[st] - 1) / C::NS) & 1, nullptr);
-                if (last_v[st]) mbar_wait(&bars->v_full[st], ((last_v[st] - 1) / C::NS) & 1, nullptr);
+                if (last_k[st]) mbar_wait_spin(&bars->k_full[st], ((last_k[st] - 1) / C::NS) & 1, nullptr);
+                if (last_v[st]) mbar_wait_spin(&bars->v_full[st], ((last_v[st] - 1) / C::NS) & 1, nullptr);
             }
         }
     } else if (warp == kWarpMma) {
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (leader) {
             tc_commit(&bars->drain);
-            mbar_wait(&bars->drain, 0, nullptr);
+            mbar_wait_spin(&bars->drain, 0, nullptr);
         }
         __syncwarp();
     } else {
