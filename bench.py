@@ -129,6 +129,16 @@ L2_BYTES = 129 * 10**6
 SIMT_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # the SIMT kernels' arithmetic bound
 
 
+def data_note(w):
+    """The `data` entry of a JSON line: how the workload's inputs are drawn."""
+    def n(std):
+        return "N(0,1)" if std == 1.0 else f"N(0,{std:g}^2)"
+    dist = (f"Q, K ~ {n(w.qk_std)}, V ~ {n(w.v_std)}, dO ~ {n(w.do_std)}" if (w.qk_std, w.v_std, w.do_std) != (1, 1, 1)
+            else "Q, K, V, dO ~ N(0,1)")
+    return (f"synthetic, seed {w.seed}: {dist}" + (", rounded to bf16" if w.dtype == "bf16" else "")
+            + "; recipe in bwd_xfa_fwd_gb300/inputs.py")
+
+
 def workload_config(w):
     elt = 2 if w.dtype == "bf16" else 4
     one = w.bh * w.S * w.hd * elt   # Q, K, V and dO, each streamed every step
@@ -277,7 +287,7 @@ def run_reference(args, w):
                   f"causal convention")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": K, "warmup": W, "ms_per_step": dt / K * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), bf16-rounded)",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": data_note(w),
             "config": workload_config(w),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
                              "sample": sample_txt},
@@ -463,8 +473,7 @@ def run_ours(args, w):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": w.dtype,
-        "data": ("synthetic (seeded N(0,1)" + (", bf16-rounded" if w.dtype == "bf16" else "")
-                 + "; recipe in bwd_xfa_fwd_gb300/inputs.py)"),
+        "data": data_note(w),
         "config": dict(workload_config(w), kernel_family=args.family,
                        **({"dropout_p": args.dropout, "dropout_seed": DROPOUT_SEED} if args.dropout else {})),
         "fwd_tflops": f_fwd / (per["fwd"] * 1e-3) / 1e12,

@@ -1,8 +1,14 @@
 """bench.py's description of what it times (CPU): the L2 note that the timing rules rest on,
 the kernel family, ceiling and launch count it reports for each dtype and head dimension,
-and the kernel-source hash that gates recorded DRAM traffic."""
+the kernel-source hash that gates recorded DRAM traffic, the input description, and the
+reference (CPU oracle) arm's JSON line."""
+import os
+
 import bench
 from bwd_xfa_fwd_gb300 import inputs
+from bwd_xfa_fwd_gb300.inputs import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def test_l2_note_follows_the_total_of_the_streamed_inputs():
@@ -59,3 +65,28 @@ def test_source_hash_ignores_comments_only():
             bench.KERNEL_SOURCES.clear()
             bench.KERNEL_SOURCES.update(saved)
     assert hashes[0] == hashes[1] and hashes[0] != hashes[2]
+
+
+def test_data_note_states_each_workloads_distribution():
+    notes = {i: bench.data_note(WORKLOADS[i]) for i in WORKLOADS}
+    assert "dO ~ N(0,0.1^2)" in notes[2] and "bf16" not in notes[2]
+    assert "Q, K ~ N(0,2^2)" in notes[4] and "rounded to bf16" in notes[4]
+    assert notes[5].startswith("synthetic, seed 5: Q, K, V, dO ~ N(0,1), rounded to bf16")
+
+
+def test_reference_arm_line_on_the_smallest_workload():
+    """`bench.py --impl reference` times the CPU oracle and prints one JSON line with the
+    contract's keys (run on workload 1, which takes well under a second)."""
+    import json
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "1",
+                        "--steps", "3", "--warmup", "3"], capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["steps"] == 3 and d["warmup"] == 3 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"] == WORKLOADS[1].name
