@@ -126,6 +126,9 @@ def dist_env():
 
 
 L2_BYTES = 129 * 10**6
+# Steps of the end-to-end leg, whatever --steps is: the first upload and the last download
+# are not overlapped with compute, so a short leg would measure the pipeline's fill and drain.
+E2E_STEPS = 64
 SIMT_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # the SIMT kernels' arithmetic bound
 
 
@@ -341,7 +344,7 @@ def measure_e2e(torch, binding, w, dev, ws, impl, K, flops, world):
     for i in range(2):
         step(i)
     torch.cuda.synchronize()
-    ke = max(4, K // 4)
+    ke = E2E_STEPS
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     for e in computed + downloaded:   # start the clock with no step in flight
@@ -353,8 +356,9 @@ def measure_e2e(torch, binding, w, dev, ws, impl, K, flops, world):
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / ke
     return {"value": flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-            "pipelining": "upload / compute / download streams, two buffer sets"}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": ke,
+            "pipelining": "upload / compute / download streams, two buffer sets; the clock runs from the first "
+                          "upload to the last download"}
 
 
 def run_ours(args, w):
@@ -460,7 +464,14 @@ def run_ours(args, w):
     k_fwd, k_bwd, launches = kernel_labels(w, rfam)
     peak_tc, peak_src = tensor_peak(pk, pk_kind, rfam)
     main_tflops = f_bwd / (per["main"] * 1e-3) / 1e12
-    prep_bytes = w.bh * w.S * (2 * w.hd * 2 + 4 + 4 + 4 + 4 * w.hd)
+    elt = 2 if w.dtype == "bf16" else 4
+    # The D pre-pass by the method's own byte count: read O and dO, write D.
+    d_bytes = w.bh * w.S * (2 * w.hd * elt + 4)
+    # What the same launch does besides, for the fused dQ route: read L, write -L*log2(e) and
+    # clear the fp32 dQ accumulator the backward kernel reduces into.
+    clears_acc = rfam in ("tc", "simt")   # the fused tcgen05 and the SIMT backward reduce dQ into fp32
+    extra_bytes = w.bh * w.S * (4 + 4 + (4 * w.hd if clears_acc else 0))
+    prep_gbs = lambda b: b / (per["prep"] * 1e-3) / 1e9   # noqa: E731
     line = {
         "metric": METRIC,
         "value": (f_fwd + f_bwd) * world / (ms_step * 1e-3) / 1e12,
@@ -474,8 +485,9 @@ def run_ours(args, w):
         "vs_baseline": None,
         "dtype": w.dtype,
         "data": data_note(w),
-        "config": dict(workload_config(w), kernel_family=args.family,
+        "config": dict(workload_config(w),
                        **({"dropout_p": args.dropout, "dropout_seed": DROPOUT_SEED} if args.dropout else {})),
+        "kernel_family": args.family,
         "fwd_tflops": f_fwd / (per["fwd"] * 1e-3) / 1e12,
         "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
         "fwd_frac_of_peak": f_fwd / (per["fwd"] * 1e-3) / 1e12 / peak_tc,
@@ -496,9 +508,13 @@ def run_ours(args, w):
                          "traffic": (recorded_traffic("tc_fwd", w.name) if rfam in ("tc", "tc_det")
                                      and not args.dropout else None)},
         "roofline_prep": None if args.dropout else {
-            "kernel": "rowdot_kernel (xfa_bwd_prep)", "bound": "hbm",
-            "achieved": prep_bytes / (per["prep"] * 1e-3) / 1e9, "peak": float(pk["hbm_gbs"]),
-            "unit": "GB/s", "frac": prep_bytes / (per["prep"] * 1e-3) / 1e9 / float(pk["hbm_gbs"]),
+            "kernel": "rowdot_kernel (xfa_bwd_prep): the D pre-pass, bytes of O, dO read and D written",
+            "bound": "hbm", "achieved": prep_gbs(d_bytes), "peak": float(pk["hbm_gbs"]), "unit": "GB/s",
+            "frac": prep_gbs(d_bytes) / float(pk["hbm_gbs"]), "bytes": d_bytes,
+            "same_launch": {"what": "L read, -L*log2(e) written" + (", fp32 dQ accumulator cleared"
+                                                                    if clears_acc else ""),
+                            "bytes": extra_bytes, "achieved_all_bytes": prep_gbs(d_bytes + extra_bytes),
+                            "frac_all_bytes": prep_gbs(d_bytes + extra_bytes) / float(pk["hbm_gbs"])},
             "traffic": recorded_traffic("rowdot", w.name)},
         "e2e": e2e,
         "graph": graph,

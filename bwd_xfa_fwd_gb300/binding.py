@@ -52,6 +52,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "xfa_rowdot": ([vp, vp, vp, i, i, i, i, vp], i),
         "xfa_accumulate": ([vp, vp, sz, i, vp], i),
         "xfa_status": ([vp], i),
+        "xfa_last_status": ([vp], i),
         "xfa_selftest_timeout": ([ctypes.c_uint, vp], i),
         "xfa_strerror": ([i], ctypes.c_char_p),
         "xfa_version": ([], i),
@@ -189,7 +190,7 @@ def accumulate_(dst, src):
 def status(device=None) -> int:
     """Synchronise the current stream and return (and clear) the device status word."""
     s = torch.cuda.current_stream(device)
-    return int(load().xfa_status(ctypes.c_void_p(s.cuda_stream)))
+    return int(load().xfa_last_status(ctypes.c_void_p(s.cuda_stream)))
 
 
 def selftest_timeout(timeout_us: int, device=None) -> int:

@@ -2,6 +2,7 @@
 // kernel translation units.  Not part of the public ABI.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -93,6 +94,23 @@ int launch_tf_bwd(const BwdParams &p, cudaStream_t st);
 
 // Streaming multiprocessors of the current device (queried once per device), for persistent grids.
 int device_sm_count();
+
+// Work-item counter slots of a persistent kernel (two words each: items claimed, CTAs finished).
+// Launches take slots round-robin so that launches in flight on different streams use different
+// slots; each launch's last CTA sets its slot back to zero.  A launch captured into a CUDA graph
+// keeps its slot for every replay, so captured launches take theirs from a separate pool: an
+// eager launch never shares a slot with a graph's, and graph replays that overlap one another
+// share a slot only after kSchedCapturedSlots captures of the same kernel.
+constexpr unsigned kSchedEagerSlots = 64;
+constexpr unsigned kSchedCapturedSlots = 448;
+constexpr unsigned kSchedSlots = kSchedEagerSlots + kSchedCapturedSlots;
+struct SchedSlots {
+    std::atomic<unsigned> eager{0};
+    std::atomic<unsigned> captured{0};
+};
+// The slot (index into a kernel's [2 * kSchedSlots] counter array) of a launch on `st`;
+// XFA_OK or an error code (a failed capture-status query).
+int sched_slot(cudaStream_t st, SchedSlots &slots, unsigned *slot);
 
 // Encodes the TMA descriptors; resolved once from the driver (xfa_api.cu).
 int encode_tmap_bf16_3d(void *tmap, const void *base, int hd, int S, int bh, int box_rows);

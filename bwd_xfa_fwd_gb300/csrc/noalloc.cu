@@ -6,14 +6,19 @@
 // its callbacks, or latency-critical code that cannot afford cudaMalloc's
 // implicit device-wide synchronisation.  This entry point needs no workspace
 // from them: the D / L*log2(e) rows and the fp32 dQ accumulator live in one
-// file-scope device array of XFA_NOALLOC_SCRATCH_BYTES, which every GPU that
-// loads the library holds until the process exits.
+// file-scope device array of XFA_NOALLOC_SCRATCH_BYTES, kept on a device until
+// the process exits.
 //
 // The array's host-side name is only a stand-in for the symbol; its device
 // address is resolved with cudaGetSymbolAddress once per device (on the
-// first call made with that device current) and passed to the kernels.  All
-// calls share the array and it keeps the last call's contents; the pre-pass
-// of every call rewrites D and L and clears the dQ accumulator before use.
+// first call made with that device current) and passed to the kernels.  With
+// lazy module loading (CUDA's default) that first resolution is also what
+// loads this file's module, and so reserves the array on the device: the
+// first call on a device may allocate and synchronise, and fails with
+// cudaErrorMemoryAllocation when the device is full.  Later calls allocate
+// nothing.  All calls share the array and it keeps the last call's contents;
+// the pre-pass of every call rewrites D and L and clears the dQ accumulator
+// before use.
 // Calls that overlap on the GPU (other streams, other host threads) race on
 // the array.
 #include <mutex>

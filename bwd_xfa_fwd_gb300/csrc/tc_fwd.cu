@@ -499,21 +499,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Work-item counters of the persistent forward: a slot per launch (two words: items claimed,
-// CTAs finished), handed out round-robin so that launches in flight on different streams use
-// different slots.  The last CTA of a launch to finish sets both words back to zero (every CTA
-// has claimed past the end of the list by then), so a slot is zero whenever a launch starts --
-// no memset on the stream, and graph replays reuse their slot.  Static memory starts at zero.
-constexpr int kSchedSlots = 64;
+// Work-item counters of the persistent forward, one slot per launch (see SchedSlots).  The
+// last CTA of a launch to finish sets both words back to zero (every CTA has claimed past the end
+// of the list by then), so a slot is zero whenever a launch starts -- no memset on the stream,
+// and graph replays reuse their slot.  Static memory starts at zero.
 __device__ unsigned g_next_item[2 * kSchedSlots];
-std::atomic<unsigned> g_next_slot{0};
+SchedSlots g_slots;
 
-int next_item_counter(unsigned **ctr)
+int next_item_counter(cudaStream_t st, unsigned **ctr)
 {
+    unsigned slot = 0;
+    int rc = sched_slot(st, g_slots, &slot);
+    if (rc != XFA_OK) return rc;
     void *base = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&base, g_next_item);
     if (e != cudaSuccess) return XFA_ERR_CUDA_BASE + (int)e;
-    *ctr = static_cast<unsigned *>(base) + 2 * (g_next_slot.fetch_add(1u) % kSchedSlots);
+    *ctr = static_cast<unsigned *>(base) + 2 * slot;
     return XFA_OK;
 }
 
@@ -532,7 +533,7 @@ int run(const FwdParams &p, cudaStream_t st)
     const int nqb = (p.S + 2 * BM - 1) / (2 * BM);
     const unsigned grid = (unsigned)std::min(nqb * p.bh, device_sm_count());   // persistent: one CTA per SM
     unsigned *ctr = nullptr;
-    if ((rc = next_item_counter(&ctr)) != XFA_OK) return rc;
+    if ((rc = next_item_counter(st, &ctr)) != XFA_OK) return rc;
     kern<<<grid, kThreads, Cfg<HD>::SMEM, st>>>(tq, tk, tv, (__nv_bfloat16 *)p.out, p.lse, p.bh, p.S,
                                                  p.scale * 1.4426950408889634f, p.status, p.drop,
                                                  head_bundle(p.bh, p.S, HD, 2, kHeadBundle), ctr);

@@ -1,7 +1,8 @@
 // C-ABI front end of libxfa.so (declared in include/xfa.h): argument
 // validation, workspace layout, TMA descriptor encoding, kernel-family
 // dispatch and the device status word.  Nothing here allocates, frees or
-// synchronises except xfa_status, which is documented to synchronise.
+// synchronises except xfa_last_status (and its older name xfa_status), which is
+// documented to synchronise.
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -163,6 +164,18 @@ int device_sm_count()
         g_sm_count[dev] = n;
     }
     return g_sm_count[dev];
+}
+
+int sched_slot(cudaStream_t st, SchedSlots &slots, unsigned *slot)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return cuda_code(e);
+    if (cs == cudaStreamCaptureStatusActive)
+        *slot = kSchedEagerSlots + slots.captured.fetch_add(1u) % kSchedCapturedSlots;
+    else
+        *slot = slots.eager.fetch_add(1u) % kSchedEagerSlots;
+    return XFA_OK;
 }
 
 // [bh][S][hd] bf16 tensor as a 3-D TMA map with boxes of 64 columns x box_rows rows,
@@ -424,7 +437,9 @@ int xfa_accumulate(void *dst, const void *src, size_t n, int dtype, void *stream
     return cuda_code(launch_accumulate(dst, src, n, dtype, static_cast<cudaStream_t>(stream)));
 }
 
-int xfa_status(void *stream)
+int xfa_status(void *stream) { return xfa_last_status(stream); }
+
+int xfa_last_status(void *stream)
 {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_code(e);

@@ -32,7 +32,7 @@
  *   - Return value: XFA_OK, or an error code.  Argument errors are detected
  *     on the host before anything is enqueued, and nothing is written.
  *     A CUDA launch error is returned as XFA_ERR_CUDA_BASE + cudaError_t.
- *     A kernel that gives up waiting on its own pipeline (see xfa_status)
+ *     A kernel that gives up waiting on its own pipeline (see xfa_last_status)
  *     leaves its outputs undefined.
  */
 #ifndef XFA_H
@@ -68,7 +68,7 @@ enum {
     XFA_OK = 0,
     XFA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, bad scale */
     XFA_ERR_UNSUPPORTED = 2,  /* valid but unsupported combination (hd, dtype, impl) */
-    XFA_ERR_TIMEOUT = 3,      /* a kernel gave up waiting on its pipeline (xfa_status) */
+    XFA_ERR_TIMEOUT = 3,      /* a kernel gave up waiting on its pipeline (xfa_last_status) */
     XFA_ERR_WORKSPACE = 4,    /* workspace missing or smaller than xfa_bwd_workspace_bytes */
     XFA_ERR_DEVICE = 5,       /* no usable device, or not an sm_103 device for tcgen05 */
     XFA_ERR_CUDA_BASE = 1000  /* + cudaError_t of a failed CUDA runtime call */
@@ -195,13 +195,21 @@ int xfa_bwd_finish(void *dq, int bh, int S, int hd, int dtype, void *workspace, 
  * the method.
  *   Arguments as xfa_bwd, without the workspace: the scratch is one
  *   file-scope device array of XFA_NOALLOC_SCRATCH_BYTES inside the library,
- *   held by every GPU that loads it until the process exits.
+ *   kept on a device until the process exits.
  *   Returns XFA_ERR_WORKSPACE when xfa_bwd_workspace_bytes() for the shape
  *   exceeds XFA_NOALLOC_SCRATCH_BYTES; otherwise as xfa_bwd.
- *   Allocates nothing (no cudaMalloc/cudaFree or allocating library call).
- *   The first call on a device, made with that device current, resolves the
- *   array's device address (cudaGetSymbolAddress); make that first call
- *   before any stream capture.
+ *   The entry point itself calls no cudaMalloc/cudaFree or allocating library
+ *   routine.  The array sits in a module of the library that CUDA loads on
+ *   first use (lazy module loading, CUDA's default): the first call on each
+ *   device, made with that device current, loads that module -- which
+ *   reserves the XFA_NOALLOC_SCRATCH_BYTES on the device and may synchronise
+ *   it -- and resolves the array's device address (cudaGetSymbolAddress).  That
+ *   first call can therefore fail with XFA_ERR_CUDA_BASE +
+ *   cudaErrorMemoryAllocation when the device is already full; make it at
+ *   set-up time (a small problem will do), before any stream capture and
+ *   outside callbacks that forbid allocation.  Later calls on that device
+ *   allocate nothing.  (With CUDA_MODULE_LOADING=EAGER the module, and the
+ *   array, are loaded with the library when the context is created.)
  *   Every call shares the array and it keeps the last call's contents (each
  *   call rewrites or clears everything it reads before reading it); calls
  *   that overlap on the GPU race on it.
@@ -232,15 +240,20 @@ int xfa_accumulate(void *dst, const void *src, size_t n, int dtype, void *stream
  * since the last call gave up on a pipeline wait (every wait in every kernel
  * has a time limit of about one second, after which the kernel records the
  * timeout, drains its own in-flight copies, frees its tensor memory and
- * exits), or XFA_ERR_CUDA_BASE + a CUDA error.
+ * exits), or XFA_ERR_CUDA_BASE + a CUDA error.  The pages' own kernels
+ * synchronise after every operation ("xtrain docs/03-autograd-engine.md",
+ * section "kernel 实现要点"); here that check is this one explicit call.
  */
+int xfa_last_status(void *stream);
+
+/* The same call under its earlier name (kept for existing callers). */
 int xfa_status(void *stream);
 
 /*
  * Self-test of the timeout path: enqueues one single-CTA kernel that waits on
  * a shared-memory barrier which nothing ever arrives on, with a limit of
  * `timeout_us` microseconds (1 .. 1000000).  The kernel then records
- * XFA_ERR_TIMEOUT in the status word and returns; read it with xfa_status.
+ * XFA_ERR_TIMEOUT in the status word and returns; read it with xfa_last_status.
  * No counterpart on the pages: it exists so the timeout path can be tested
  * without hanging a GPU.
  */

@@ -17,9 +17,10 @@ softmax-backward identities of "xtrain docs/13-flash-attention.md"
 differences in fp64, special cases with closed forms (S=1, Q=0, hd=1) and the
 unmasked case against a dense numpy softmax.  The optional dropout on the
 attention probabilities ("xtrain docs/17-dropout.md", section "Key Design
-Decisions") is pinned by ``tests/test_oracle_dropout.py``: known outputs of the
-SplitMix64 generator, the keep rate, p = 0 against the plain path, finite
-differences with the mask fixed, the D identity and the expectation over seeds.
+Decisions") is pinned by ``DROPOUT_PINS`` in ``tests/oracle_pins.py`` (run by
+``tests/test_oracle.py``): known outputs of the SplitMix64 generator, the keep
+rate, p = 0 against the plain path, finite differences with the mask fixed, the
+D identity and the expectation over seeds.
 """
 from __future__ import annotations
 

@@ -90,3 +90,5 @@ def test_reference_arm_line_on_the_smallest_workload():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["config"]["workload"] == WORKLOADS[1].name
+    # the same config object as the repo arm's line (no family or other run options in it)
+    assert d["config"] == bench.workload_config(WORKLOADS[1])

@@ -1,10 +1,12 @@
 """Edge cases of the CUDA path against the CPU oracle (GB300 only): score shapes that
-drive the online softmax's running maximum, the largest problem the boundary
-accepts, and the rejection of the first shape past it.  Every call goes through
+drive the online softmax's running maximum, near-parallel keys (dQ as a near
+cancellation), the largest problem the boundary accepts, and the rejection of the
+first shape past it.  Every call goes through
 the C ABI (ctypes binding)."""
 import ctypes
 import math
 
+import numpy as np
 import pytest
 import torch
 
@@ -36,6 +38,35 @@ def test_running_max_patterns(pattern, dtype, hd, impl):
     got = run_gpu(x, dtype, scale, impl=impl)
     ref = oracle_result(("pattern", pattern, hd, dtype), x, scale)
     compare(got, ref, dtype)
+
+
+# Near-parallel keys: the "rising" pattern with no spread in the other coordinates of K,
+# so every key of a row's softmax window lies in one plane at nearly the same angle.  Then
+# dQ_i = sum_j dS_ij K_j = sum_j dS_ij (K_j - K_i) (rows of dS sum to zero) is a near
+# cancellation, and rounding dS to bf16 -- the operand of the dQ contraction in every bf16
+# tensor-core backward -- costs up to sum_j |dS_ij| |K_jd| 2^-8 per element (bf16 keeps 8
+# significant bits), 7-8 % of max|dQ| on these inputs (4-7 % measured by rounding the
+# oracle's own dS).  The test asserts every other output at the usual tolerance and dQ
+# element by element within that rounding bound on top of it.
+@pytest.mark.parametrize("hd,impl", [(128, 2), (64, 2), (128, 3), (64, 3)])
+def test_near_parallel_keys(hd, impl):
+    bh, S = 2, 1000
+    scale = 1.0 / math.sqrt(hd)
+    x = inputs.patterned((bh, S, hd), "bf16", "rising", seed=77 + hd, k_noise=0.0)
+    got = run_gpu(x, "bf16", scale, impl=impl)
+    ref = oracle_result(("parallel", hd), x, scale)
+    compare(got, ref, "bf16", names=("out", "lse", "dk", "dv"))
+    tol = TOL["bf16"]["rel"]
+    mask = np.tril(np.ones((S, S), dtype=bool))
+    for b in range(bh):
+        q, k, v, do = (x[n].exact[b] for n in ("q", "k", "v", "dout"))
+        s = np.where(mask, scale * (q @ k.T), 0.0)
+        p = np.where(mask, np.exp(s - ref["lse"][b][:, None]), 0.0)
+        ds = scale * p * (do @ v.T - np.sum(do * ref["out"][b], axis=1)[:, None])
+        rounding = 2.0 ** -8 * (np.abs(ds) @ np.abs(k))
+        err = np.abs(got["dq"][b] - ref["dq"][b])
+        bound = tol * np.max(np.abs(ref["dq"][b])) + rounding
+        assert np.all(err <= bound), f"head {b}: dQ error exceeds the bf16 rounding bound by {np.max(err - bound):.3e}"
 
 
 # The boundary accepts bh * S * hd < 2^31 elements.  At the largest such bh (S = 1024,

@@ -97,3 +97,62 @@ def test_concurrent_streams_and_counter_reuse():
         for c, o in zip(cases, outs):
             for a, b in zip(c["ref"], o):
                 assert torch.equal(a, b), f"repetition {rep}"
+
+
+def test_graph_replays_overlapping_eager_launches():
+    """A captured launch keeps its work-counter slot for every replay; eager launches take
+    theirs from another pool.  Replays of a captured forward + backward on one stream, with
+    more eager launches than the eager pool has slots running on a second stream at the same
+    time, both give the results of a lone launch."""
+    from bwd_xfa_fwd_gb300 import binding
+    bh, S, hd = 4, 1000, 128
+    scale = 1.0 / math.sqrt(hd)
+    impl = binding.IMPL_TCGEN05_DET
+    cases = []
+    for i in range(2):
+        x = inputs.draw((bh, S, hd), "bf16", seed=700 + i)
+        q, k, v, do = (to_device(x[n], "bf16") for n in ("q", "k", "v", "dout"))
+        out, lse = binding.fwd(q, k, v, scale, impl)
+        grads = binding.bwd(q, k, v, out, do, lse, scale, impl)
+        torch.cuda.synchronize()
+        cases.append(dict(qkvd=(q, k, v, do), ref=[t.clone() for t in (out, lse) + tuple(grads)]))
+    q, k, v, do = cases[0]["qkvd"]
+    out, lse = torch.empty_like(q), torch.empty(bh, S, device="cuda", dtype=torch.float32)
+    grads = tuple(torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(binding.workspace_bytes(bh, S, hd, q.dtype), device="cuda", dtype=torch.uint8)
+
+    def step():
+        binding.fwd(q, k, v, scale, impl, out=out, lse=lse)
+        binding.bwd(q, k, v, out, do, lse, scale, impl, workspace=ws, grads=grads)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    replay_stream, eager_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    for t in (replay_stream, eager_stream):
+        t.wait_stream(torch.cuda.current_stream())
+    eager_outs = []
+    for rep in range(70):   # 70 x 2 eager persistent launches: every eager slot is taken twice
+        with torch.cuda.stream(replay_stream):
+            g.replay()
+        with torch.cuda.stream(eager_stream):
+            qb, kb, vb, dob = cases[1]["qkvd"]
+            ob, lb = binding.fwd(qb, kb, vb, scale, impl)
+            gb = binding.bwd(qb, kb, vb, ob, dob, lb, scale, impl)
+            if rep % 10 == 9:
+                eager_outs.append((ob, lb) + tuple(gb))
+        if rep % 10 == 9:
+            replay_stream.synchronize()
+            for a, b in zip(cases[0]["ref"], (out, lse) + grads):
+                assert torch.equal(a, b), f"replay {rep}"
+    torch.cuda.synchronize()
+    assert binding.status() == binding.XFA_OK
+    for o in eager_outs:
+        for a, b in zip(cases[1]["ref"], o):
+            assert torch.equal(a, b)

@@ -6,8 +6,10 @@ inside the library instead of a caller-provided workspace.
 
 Checked through the C ABI against xfa_bwd on the same inputs, on two calls in
 a row (the array keeps the previous call's contents, so the second call shows
-that everything read is rewritten or cleared first).  This file is collected
-last so that a run stopping at the first failure has run every other test."""
+that everything read is rewritten or cleared first), and the second call is
+checked to leave the device's free memory and torch's allocator unchanged.
+This file is collected last so that a run stopping at the first failure has
+run every other test."""
 import ctypes
 import math
 
@@ -50,8 +52,15 @@ def test_noalloc_matches_bwd_twice(lib, dtype, hd, S, bh):
         t["out"], t["lse"] = binding.fwd(t["q"], t["k"], t["v"], scale)
         want = binding.bwd(t["q"], t["k"], t["v"], t["out"], t["dout"], t["lse"], scale)
         got = tuple(torch.full_like(t["q"], float("nan")) for _ in range(3))
+        torch.cuda.synchronize()
+        free0, held0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
         assert _call(lib, t, got, bh, S, hd, scale, code) == binding.XFA_OK
         torch.cuda.synchronize()
+        if call == 1:
+            # the first call on a device may load the library module that holds the array;
+            # a later call must leave the device's free memory and torch's allocator as they were
+            assert torch.cuda.mem_get_info()[0] == free0
+            assert torch.cuda.memory_allocated() == held0
         assert binding.status() == binding.XFA_OK
         compare({n: to_f64(g) for n, g in zip(("dq", "dk", "dv"), got)},
                 {n: to_f64(w) for n, w in zip(("dq", "dk", "dv"), want)}, dtype, names=("dq", "dk", "dv"))
