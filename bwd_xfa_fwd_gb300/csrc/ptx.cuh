@@ -199,6 +199,20 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Register re-allocation between warpgroups (all four warps of a warpgroup execute it).  The
+// sum over the CTA must stay within what the CTA was launched with; an increase waits until
+// other warpgroups have released enough registers.
+template <uint32_t N>
+__device__ __forceinline__ void regs_increase()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_decrease()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols)

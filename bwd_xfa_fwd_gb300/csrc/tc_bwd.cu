@@ -49,15 +49,29 @@ namespace {
 
 constexpr int BN = 128;       // keys per CTA (MMA M)
 constexpr int BM = 64;        // query rows per tile (MMA N of S^T / dP^T)
-template <int HD>
-constexpr int ring_depth() { return HD == 128 ? 3 : 4; }   // query-tile (Q, dO, L, D) ring stages
+// query-tile (Q, dO, L, D) ring stages; with dropout at hd = 128 two, to make room for the keep bits
+template <int HD, bool DROP>
+constexpr int ring_depth() { return HD == 128 ? (DROP ? 2 : 3) : 4; }
 constexpr int kThreads = 320;
 constexpr int kWarpTma = 8, kWarpMma = 9;
+// With dropout: 16 warps.  Warps 12-15 draw the keep bits of every (key, query row) of the
+// coming query tiles into shared memory (MSB stages), so the key-row warps only read them; warps
+// 10-11 are idle.  Registers: the key-row warpgroup grows to 200, the TMA/MMA/idle warpgroup
+// shrinks to 56 and the mask warpgroup to 96, the readout warpgroup keeps the 128 of a 512-thread
+// launch (200 + 128 + 56 + 96 <= 512 per lane of a warpgroup).
+constexpr int kThreadsDrop = 512;
+constexpr int kWarpMask0 = 12;
+constexpr int MSB = 4;   // keep-bit stages (query tiles)
+
+struct MaskBars {
+    uint64_t full[MSB];    // keep bits of a query tile written (one arrival per mask warp)
+    uint64_t empty[MSB];   // read by the key-row warps (one arrival per warp)
+};
 constexpr int kHeadBundle = 4;   // heads scheduled together at long S (L2 reuse of inputs and dQ accumulator)
 
-template <int HD>
+template <int HD, bool DROP = false>
 struct Cfg {
-    static constexpr int NSQ = ring_depth<HD>();
+    static constexpr int NSQ = ring_depth<HD, DROP>();
     static constexpr int SUB = HD / 64;
     static constexpr int KV_SUB = BN * 128;             // 128 rows x 128 B
     static constexpr int Q_SUB = BM * 128;              // 64 rows x 128 B
@@ -71,7 +85,10 @@ struct Cfg {
     static constexpr int OFF_DS = OFF_DO + NSQ * Q_BYTES;
     static constexpr int OFF_DQ = OFF_DS + 2 * DS_BYTES;  // fp32 dQ tile [64 rows][hd] staged for the bulk reduce
     static constexpr int OFF_LD = OFF_DQ + BM * HD * 4;   // per stage: Lg[64], D[64]
-    static constexpr int OFF_BAR = OFF_LD + NSQ * 2 * BM * 4;
+    // dropout: keep bits [stage][key] x 64 query rows, then their barriers
+    static constexpr int OFF_MASK = OFF_LD + NSQ * 2 * BM * 4;
+    static constexpr int OFF_MBAR = OFF_MASK + (DROP ? MSB * BN * 8 : 0);
+    static constexpr int OFF_BAR = OFF_MBAR + (DROP ? 128 : 0);
     static constexpr int SMEM = OFF_BAR + 256 + 1024;   // barriers + alignment slack
     // TMEM columns: dK, dV accumulators; S^T (P^T bf16 written back into its first 32 columns);
     // dP^T (dS^T bf16 written back into its first 32 columns); dQ^T; K_j as a bf16 A operand.
@@ -186,7 +203,7 @@ __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t k_tmem, uint64
 // DROP: dropout on the attention probabilities (fused only): dV takes P o C and dS is
 // formed from C o dP, with C re-drawn from (seed, flat index).
 template <int HD, bool FUSED_DQ, bool DROP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const float *__restrict__ Lg, const float *__restrict__ Dg, float *__restrict__ dq_acc,
@@ -194,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   float scale, float scale_log2, int *status, const DropParams drop, int bundle_heads,
                   unsigned *__restrict__ next_item)
 {
-    using C = Cfg<HD>;
+    using C = Cfg<HD, DROP>;
     constexpr int NSQ = C::NSQ;
     constexpr bool TWO_S = C::template two_s<FUSED_DQ>();
     static_assert(NSQ <= kMaxRing && sizeof(Bars) <= 256, "barrier block");
@@ -242,7 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->ds_full[b], 4);   // one arrival per key warp
             mbar_init(&bars->ds_empty[b], 1);
             mbar_init(&bars->item_full[b], 1);
-            mbar_init(&bars->item_empty[b], 9);   // MMA warp, four key warps, four readout warps
+            // MMA warp, four key warps, four readout warps (+ four mask warps)
+            mbar_init(&bars->item_empty[b], 9 + (DROP ? 4 : 0));
         }
         mbar_init(&bars->s_full[0], 1);
         mbar_init(&bars->s_full[1], 1);
@@ -254,6 +272,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->done, 1);
         mbar_init(&bars->dk_read, 4);         // one arrival per readout warp
         mbar_init(&bars->drain, 1);
+        if (DROP) {
+            MaskBars *mb = reinterpret_cast<MaskBars *>(smem + C::OFF_MBAR);
+            for (int s = 0; s < MSB; ++s) {
+                mbar_init(&mb->full[s], 4);
+                mbar_init(&mb->empty[s], 4);
+            }
+        }
         bars->abort = 0;
         fence_barrier_init();
     }
@@ -266,183 +291,232 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp == kWarpTma) {
-        if (lane == 0) {
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-            prefetch_tensormap(&tm_q);
-            prefetch_tensormap(&tm_do);
-            uint32_t gt = 0;                      // query tiles issued
-            uint32_t last[kMaxRing] = {};         // 1 + last tile issued per stage
-            int kv_loads = 0;
+    MaskBars *mbars = reinterpret_cast<MaskBars *>(smem + C::OFF_MBAR);
+    const uint32_t *mask_s = reinterpret_cast<const uint32_t *>(smem + C::OFF_MASK);
+
+    // Roles by warpgroup (with dropout every warpgroup first resizes its registers, all four warps
+    // together): warps 8-11 the TMA and MMA warps (and two idle ones), 12-15 the keep-bit warps,
+    // 0-3 the key-row warps, 4-7 the dQ readout warps.
+    if (warp >= 8 && warp < 12) {
+        if (DROP) regs_decrease<56>();
+        if (warp == kWarpTma) {
+            if (lane == 0) {
+                prefetch_tensormap(&tm_k);
+                prefetch_tensormap(&tm_v);
+                prefetch_tensormap(&tm_q);
+                prefetch_tensormap(&tm_do);
+                uint32_t gt = 0;                      // query tiles issued
+                uint32_t last[kMaxRing] = {};         // 1 + last tile issued per stage
+                int kv_loads = 0;
+                bool ok = true;
+                for (int kc = 0; ok; ++kc) {          // kc: items claimed, posted in ring entry kc & 1
+                    const int e = kc & 1;
+                    if (kc >= 2 && !(ok = mbar_wait(&bars->item_empty[e], ((kc >> 1) + 1) & 1, &bars->abort))) break;
+                    int item = (int)atomicAdd(next_item, 1u);
+                    if (item >= n_items) item = -1;
+                    *reinterpret_cast<volatile int *>(&bars->item_id[e]) = item;
+                    mbar_arrive(&bars->item_full[e]);
+                    if (item < 0) break;
+                    const Item w = item_of(item);
+                    // K, V of this item: their buffers are free once the previous item's MMAs are done
+                    if (kc > 0 && !(ok = mbar_wait(&bars->done, (kc - 1) & 1, &bars->abort))) break;
+                    mbar_arrive_expect_tx(&bars->kv_full, 2 * C::KV_BYTES);
+                    for (int s = 0; s < C::SUB; ++s) {
+                        tma_load_3d(smem + C::OFF_K + s * C::KV_SUB, &tm_k, &bars->kv_full, s * 64, w.j0, w.head);
+                        tma_load_3d(smem + C::OFF_V + s * C::KV_SUB, &tm_v, &bars->kv_full, s * 64, w.j0, w.head);
+                    }
+                    ++kv_loads;
+                    for (int it = 0; it < w.n; ++it) {
+                        const uint32_t gi = gt + it;
+                        const int st = gi % NSQ;
+                        if (gi >= NSQ && !(ok = mbar_wait(&bars->q_empty[st], ((gi / NSQ) + 1) & 1, &bars->abort))) break;
+                        const int i0 = (w.it0 + it) * BM;
+                        mbar_arrive_expect_tx(&bars->q_full[st], 2 * C::Q_BYTES + 2 * BM * 4);
+                        for (int s = 0; s < C::SUB; ++s) {
+                            tma_load_3d(smem + C::OFF_Q + st * C::Q_BYTES + s * C::Q_SUB, &tm_q, &bars->q_full[st],
+                                        s * 64, i0, w.head);
+                            tma_load_3d(smem + C::OFF_DO + st * C::Q_BYTES + s * C::Q_SUB, &tm_do, &bars->q_full[st],
+                                        s * 64, i0, w.head);
+                        }
+                        float *ld = ld_s + st * 2 * BM;
+                        bulk_load(ld, Lg + (size_t)w.head * S_pad + i0, BM * 4, &bars->q_full[st]);
+                        bulk_load(ld + BM, Dg + (size_t)w.head * S_pad + i0, BM * 4, &bars->q_full[st]);
+                        last[st] = gi + 1;
+                    }
+                    gt += w.n;
+                }
+                if (!ok) fail(bars, status);
+                // Never leave the CTA with copies in flight: wait for the last load of K/V and of each stage.
+                if (kv_loads > 0) mbar_wait(&bars->kv_full, (kv_loads - 1) & 1, nullptr);
+                for (int st = 0; st < NSQ; ++st)
+                    if (last[st]) mbar_wait(&bars->q_full[st], ((last[st] - 1) / NSQ) & 1, nullptr);
+            }
+        } else if (warp == kWarpMma) {
+            // The whole warp runs the issue loop (converged, descriptors warp-uniform);
+            // one elected lane issues the tcgen05 instructions.
+            const bool leader = elect_one();
+            const uint32_t k_s = smem_u32(smem + C::OFF_K), v_s = smem_u32(smem + C::OFF_V);
+            const uint32_t q_s = smem_u32(smem + C::OFF_Q), do_s = smem_u32(smem + C::OFF_DO);
+            const uint32_t ds_s = smem_u32(smem + C::OFF_DS);
+            // K-major views (hd contiguous) for dP^T = V dO^T and the B operand Q_i of S^T
+            const uint64_t v_km = sdesc_sw128(v_s, 16, 1024);
+            const uint64_t q_km = sdesc_sw128(q_s, 16, 1024), do_km = sdesc_sw128(do_s, 16, 1024);
+            // MN-major views: B = dO_i / Q_i for dV / dK, A = K_j^T for dQ^T; dS^T as K-major A / MN-major B
+            const uint64_t do_mn = sdesc_sw128(do_s, C::Q_SUB, 1024), q_mn = sdesc_sw128(q_s, C::Q_SUB, 1024);
+            const uint64_t k_mn = sdesc_sw128(k_s, C::KV_SUB, 1024);
+            const uint64_t ds_mn = sdesc_sw128(ds_s, C::DS_BYTES, 1024);
+            constexpr uint32_t idesc_acc = idesc_bf16(BN, HD, false, true);    // dV, dK: B MN-major
+            constexpr uint32_t idesc_dq = idesc_bf16(128, BM, true, true);     // dQ^T: A, B MN-major
+            constexpr uint32_t idesc_s = idesc_bf16(BN, BM, false, false);     // S^T: A = K_j from TMEM
+            uint32_t gt = 0;   // query tiles of earlier items
             bool ok = true;
-            for (int kc = 0; ok; ++kc) {          // kc: items claimed, posted in ring entry kc & 1
-                const int e = kc & 1;
-                if (kc >= 2 && !(ok = mbar_wait(&bars->item_empty[e], ((kc >> 1) + 1) & 1, &bars->abort))) break;
-                int item = (int)atomicAdd(next_item, 1u);
-                if (item >= n_items) item = -1;
-                *reinterpret_cast<volatile int *>(&bars->item_id[e]) = item;
-                mbar_arrive(&bars->item_full[e]);
+            for (int k = 0; ok; ++k) {
+                const int item = take_item(bars, k, status, ok);
+                if (item < 0) break;
+                const int n = item_of(item).n;
+                const int st0 = gt % NSQ;
+                ok = warp_wait(&bars->kv_full, k & 1, bars, status) && warp_wait(&bars->kt_full, k & 1, bars, status) &&
+                     warp_wait(&bars->q_full[st0], (gt / NSQ) & 1, bars, status);
+                if (!ok) break;
+                tc_fence_after_sync();
+                if (leader) {
+                    // the S^T / dP^T columns last held the previous item's final P^T / dS^T, read by
+                    // its dV / dK MMAs issued before (in order)
+                    issue_s<HD>(tmem + C::template col_s<FUSED_DQ>(gt), tmem + C::COL_KT,
+                                sdesc_advance(q_km, st0 * C::Q_BYTES), idesc_s);
+                    tc_commit(&bars->s_full[TWO_S ? (gt & 1) : 0]);
+                    issue_rows_dot<HD>(tmem + C::COL_DP, v_km, sdesc_advance(do_km, st0 * C::Q_BYTES));
+                    tc_commit(&bars->dp_full);
+                }
+                __syncwarp();
+                for (int it = 0; ok && it < n; ++it) {
+                    const uint32_t gi = gt + it;
+                    const int b = gi & 1, st = gi % NSQ;
+                    const uint32_t ph2 = (gi >> 1) & 1;
+                    const uint32_t qoff = st * C::Q_BYTES, dsoff = b * C::DS_BYTES;
+                    const int nx = it + 1;
+                    const uint32_t gn = gi + 1;
+                    const int stn = gn % NSQ;
+                    // Next S^T.  With two S^T buffers it goes first, into the other one, so that it
+                    // does not queue behind this tile's work (that buffer's P^T, tile gi - 1, was read by
+                    // the dV MMA issued one iteration ago, and the in-order pipe runs that MMA first).
+                    // With one buffer it follows this tile's dV, which reads P^T from the same columns.
+                    const bool s_first = TWO_S && nx < n;
+                    if (s_first) {
+                        if (!(ok = warp_wait(&bars->q_full[stn], (gn / NSQ) & 1, bars, status))) break;
+                        tc_fence_after_sync();
+                        if (leader) {
+                            issue_s<HD>(tmem + C::template col_s<FUSED_DQ>(gn), tmem + C::COL_KT, sdesc_advance(q_km, stn * C::Q_BYTES),
+                                        idesc_s);
+                            tc_commit(&bars->s_full[gn & 1]);
+                        }
+                        __syncwarp();
+                    }
+                    // dV += P^T dO_i  (P^T: bf16 in the first columns of this tile's S^T).  The item's
+                    // first dV overwrites the accumulator, which the key warps have read out before
+                    // they wrote this P^T.
+                    if (!(ok = warp_wait(&bars->p_full, gi & 1, bars, status))) break;
+                    tc_fence_after_sync();
+                    if (leader) {
+    #pragma unroll
+                        for (int ks = 0; ks < BM / 16; ++ks)
+                            mma_ts(tmem + C::COL_DV, tmem + C::template col_s<FUSED_DQ>(gi) + ks * 8,
+                                   sdesc_advance(do_mn, qoff + ks * 2048), idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
+                    }
+                    __syncwarp();
+                    if (!TWO_S && nx < n) {   // next S^T: its columns are free once the dV MMA above has read P^T
+                        if (!(ok = warp_wait(&bars->q_full[stn], (gn / NSQ) & 1, bars, status))) break;
+                        tc_fence_after_sync();
+                        if (leader) {
+                            issue_s<HD>(tmem + C::COL_S, tmem + C::COL_KT, sdesc_advance(q_km, stn * C::Q_BYTES), idesc_s);
+                            tc_commit(&bars->s_full[0]);
+                        }
+                        __syncwarp();
+                    }
+                    // dS^T is in TMEM (first columns of dP^T) and in smem: dK first (reads the TMEM copy),
+                    // then the next dP^T may overwrite those columns.  The item's first dK overwrites the
+                    // accumulator: the readout warps must have read the previous item's dK out of it.
+                    if (!(ok = warp_wait(&bars->ds_full[b], ph2, bars, status))) break;
+                    if (it == 0 && k > 0 && !(ok = warp_wait(&bars->dk_read, (k - 1) & 1, bars, status))) break;
+                    tc_fence_after_sync();
+                    if (leader) {
+    #pragma unroll
+                        for (int ks = 0; ks < BM / 16; ++ks)
+                            mma_ts(tmem + C::COL_DK, tmem + C::COL_DP + ks * 8, sdesc_advance(q_mn, qoff + ks * 2048),
+                                   idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
+                        tc_commit(&bars->q_empty[st]);
+                        if (nx < n) {
+                            issue_rows_dot<HD>(tmem + C::COL_DP, v_km, sdesc_advance(do_km, stn * C::Q_BYTES));
+                            tc_commit(&bars->dp_full);
+                        }
+                    }
+                    __syncwarp();
+                    if (FUSED_DQ) {
+                        if (gi > 0 && !(ok = warp_wait(&bars->dq_empty, (gi - 1) & 1, bars, status))) break;
+                        tc_fence_after_sync();
+                        if (leader) {
+    #pragma unroll
+                            for (int ks = 0; ks < BN / 16; ++ks)
+                                mma_ss(tmem + C::COL_DQ, sdesc_advance(k_mn, ks * 2048),
+                                       sdesc_advance(ds_mn, dsoff + ks * 2048), idesc_dq, ks > 0 ? 1u : 0u);
+                            tc_commit(&bars->dq_full);
+                            tc_commit(&bars->ds_empty[b]);
+                        }
+                        __syncwarp();
+                    }
+                }
+                if (!ok) break;
+                if (leader) tc_commit(&bars->done);   // every MMA of this item (K, V, the accumulators)
+                __syncwarp();
+                gt += n;
+            }
+            if (leader) {
+                tc_commit(&bars->drain);
+                mbar_wait(&bars->drain, 0, nullptr);
+            }
+            __syncwarp();
+        }
+    } else if (warp >= 12) {
+        if (DROP) {
+            regs_decrease<96>();
+            // keep bits (dropout): thread = key r of the item's key tile; for every query tile, in
+            // the order the key-row warps consume them, the 64 decisions of (row i0 + c, key) as two
+            // 32-bit words, element drawn from its flat index (head*S + i0 + c)*S + key
+            const int r = (warp - kWarpMask0) * 32 + lane;
+            uint32_t *mask_w = reinterpret_cast<uint32_t *>(smem + C::OFF_MASK);
+            uint32_t nm = 0;   // stages filled
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int item = take_item(bars, k, status, ok);
                 if (item < 0) break;
                 const Item w = item_of(item);
-                // K, V of this item: their buffers are free once the previous item's MMAs are done
-                if (kc > 0 && !(ok = mbar_wait(&bars->done, (kc - 1) & 1, &bars->abort))) break;
-                mbar_arrive_expect_tx(&bars->kv_full, 2 * C::KV_BYTES);
-                for (int s = 0; s < C::SUB; ++s) {
-                    tma_load_3d(smem + C::OFF_K + s * C::KV_SUB, &tm_k, &bars->kv_full, s * 64, w.j0, w.head);
-                    tma_load_3d(smem + C::OFF_V + s * C::KV_SUB, &tm_v, &bars->kv_full, s * 64, w.j0, w.head);
-                }
-                ++kv_loads;
+                const uint64_t key = (uint64_t)(w.j0 + r);
+                const uint64_t step = (uint64_t)S * kDropGolden;
                 for (int it = 0; it < w.n; ++it) {
-                    const uint32_t gi = gt + it;
-                    const int st = gi % NSQ;
-                    if (gi >= NSQ && !(ok = mbar_wait(&bars->q_empty[st], ((gi / NSQ) + 1) & 1, &bars->abort))) break;
-                    const int i0 = (w.it0 + it) * BM;
-                    mbar_arrive_expect_tx(&bars->q_full[st], 2 * C::Q_BYTES + 2 * BM * 4);
-                    for (int s = 0; s < C::SUB; ++s) {
-                        tma_load_3d(smem + C::OFF_Q + st * C::Q_BYTES + s * C::Q_SUB, &tm_q, &bars->q_full[st],
-                                    s * 64, i0, w.head);
-                        tma_load_3d(smem + C::OFF_DO + st * C::Q_BYTES + s * C::Q_SUB, &tm_do, &bars->q_full[st],
-                                    s * 64, i0, w.head);
-                    }
-                    float *ld = ld_s + st * 2 * BM;
-                    bulk_load(ld, Lg + (size_t)w.head * S_pad + i0, BM * 4, &bars->q_full[st]);
-                    bulk_load(ld + BM, Dg + (size_t)w.head * S_pad + i0, BM * 4, &bars->q_full[st]);
-                    last[st] = gi + 1;
-                }
-                gt += w.n;
-            }
-            if (!ok) fail(bars, status);
-            // Never leave the CTA with copies in flight: wait for the last load of K/V and of each stage.
-            if (kv_loads > 0) mbar_wait(&bars->kv_full, (kv_loads - 1) & 1, nullptr);
-            for (int st = 0; st < NSQ; ++st)
-                if (last[st]) mbar_wait(&bars->q_full[st], ((last[st] - 1) / NSQ) & 1, nullptr);
-        }
-    } else if (warp == kWarpMma) {
-        // The whole warp runs the issue loop (converged, descriptors warp-uniform);
-        // one elected lane issues the tcgen05 instructions.
-        const bool leader = elect_one();
-        const uint32_t k_s = smem_u32(smem + C::OFF_K), v_s = smem_u32(smem + C::OFF_V);
-        const uint32_t q_s = smem_u32(smem + C::OFF_Q), do_s = smem_u32(smem + C::OFF_DO);
-        const uint32_t ds_s = smem_u32(smem + C::OFF_DS);
-        // K-major views (hd contiguous) for dP^T = V dO^T and the B operand Q_i of S^T
-        const uint64_t v_km = sdesc_sw128(v_s, 16, 1024);
-        const uint64_t q_km = sdesc_sw128(q_s, 16, 1024), do_km = sdesc_sw128(do_s, 16, 1024);
-        // MN-major views: B = dO_i / Q_i for dV / dK, A = K_j^T for dQ^T; dS^T as K-major A / MN-major B
-        const uint64_t do_mn = sdesc_sw128(do_s, C::Q_SUB, 1024), q_mn = sdesc_sw128(q_s, C::Q_SUB, 1024);
-        const uint64_t k_mn = sdesc_sw128(k_s, C::KV_SUB, 1024);
-        const uint64_t ds_mn = sdesc_sw128(ds_s, C::DS_BYTES, 1024);
-        constexpr uint32_t idesc_acc = idesc_bf16(BN, HD, false, true);    // dV, dK: B MN-major
-        constexpr uint32_t idesc_dq = idesc_bf16(128, BM, true, true);     // dQ^T: A, B MN-major
-        constexpr uint32_t idesc_s = idesc_bf16(BN, BM, false, false);     // S^T: A = K_j from TMEM
-        uint32_t gt = 0;   // query tiles of earlier items
-        bool ok = true;
-        for (int k = 0; ok; ++k) {
-            const int item = take_item(bars, k, status, ok);
-            if (item < 0) break;
-            const int n = item_of(item).n;
-            const int st0 = gt % NSQ;
-            ok = warp_wait(&bars->kv_full, k & 1, bars, status) && warp_wait(&bars->kt_full, k & 1, bars, status) &&
-                 warp_wait(&bars->q_full[st0], (gt / NSQ) & 1, bars, status);
-            if (!ok) break;
-            tc_fence_after_sync();
-            if (leader) {
-                // the S^T / dP^T columns last held the previous item's final P^T / dS^T, read by
-                // its dV / dK MMAs issued before (in order)
-                issue_s<HD>(tmem + C::template col_s<FUSED_DQ>(gt), tmem + C::COL_KT,
-                            sdesc_advance(q_km, st0 * C::Q_BYTES), idesc_s);
-                tc_commit(&bars->s_full[TWO_S ? (gt & 1) : 0]);
-                issue_rows_dot<HD>(tmem + C::COL_DP, v_km, sdesc_advance(do_km, st0 * C::Q_BYTES));
-                tc_commit(&bars->dp_full);
-            }
-            __syncwarp();
-            for (int it = 0; ok && it < n; ++it) {
-                const uint32_t gi = gt + it;
-                const int b = gi & 1, st = gi % NSQ;
-                const uint32_t ph2 = (gi >> 1) & 1;
-                const uint32_t qoff = st * C::Q_BYTES, dsoff = b * C::DS_BYTES;
-                const int nx = it + 1;
-                const uint32_t gn = gi + 1;
-                const int stn = gn % NSQ;
-                // Next S^T.  With two S^T buffers it goes first, into the other one, so that it
-                // does not queue behind this tile's work (that buffer's P^T, tile gi - 1, was read by
-                // the dV MMA issued one iteration ago, and the in-order pipe runs that MMA first).
-                // With one buffer it follows this tile's dV, which reads P^T from the same columns.
-                const bool s_first = TWO_S && nx < n;
-                if (s_first) {
-                    if (!(ok = warp_wait(&bars->q_full[stn], (gn / NSQ) & 1, bars, status))) break;
-                    tc_fence_after_sync();
-                    if (leader) {
-                        issue_s<HD>(tmem + C::template col_s<FUSED_DQ>(gn), tmem + C::COL_KT, sdesc_advance(q_km, stn * C::Q_BYTES),
-                                    idesc_s);
-                        tc_commit(&bars->s_full[gn & 1]);
-                    }
-                    __syncwarp();
-                }
-                // dV += P^T dO_i  (P^T: bf16 in the first columns of this tile's S^T).  The item's
-                // first dV overwrites the accumulator, which the key warps have read out before
-                // they wrote this P^T.
-                if (!(ok = warp_wait(&bars->p_full, gi & 1, bars, status))) break;
-                tc_fence_after_sync();
-                if (leader) {
+                    const uint32_t st = nm % MSB;
+                    if (nm >= MSB && !(ok = warp_wait(&mbars->empty[st], ((nm / MSB) + 1) & 1, bars, status))) break;
+                    const uint64_t i0 = (uint64_t)((w.it0 + it) * BM);
+                    uint64_t g = (((uint64_t)w.head * S + i0) * (uint64_t)S + key) * kDropGolden;
+                    uint32_t km[2];
 #pragma unroll
-                    for (int ks = 0; ks < BM / 16; ++ks)
-                        mma_ts(tmem + C::COL_DV, tmem + C::template col_s<FUSED_DQ>(gi) + ks * 8,
-                               sdesc_advance(do_mn, qoff + ks * 2048), idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
-                }
-                __syncwarp();
-                if (!TWO_S && nx < n) {   // next S^T: its columns are free once the dV MMA above has read P^T
-                    if (!(ok = warp_wait(&bars->q_full[stn], (gn / NSQ) & 1, bars, status))) break;
-                    tc_fence_after_sync();
-                    if (leader) {
-                        issue_s<HD>(tmem + C::COL_S, tmem + C::COL_KT, sdesc_advance(q_km, stn * C::Q_BYTES), idesc_s);
-                        tc_commit(&bars->s_full[0]);
+                    for (int q = 0; q < 2; ++q) {
+                        uint32_t bits = 0u;
+#pragma unroll 8
+                        for (int b = 0; b < 32; ++b) {
+                            bits |= (uint32_t)drop_keep(drop.seed, g, drop.keep_thr) << b;
+                            g += step;
+                        }
+                        km[q] = bits;
                     }
+                    *reinterpret_cast<uint2 *>(mask_w + (st * BN + r) * 2) = make_uint2(km[0], km[1]);
                     __syncwarp();
-                }
-                // dS^T is in TMEM (first columns of dP^T) and in smem: dK first (reads the TMEM copy),
-                // then the next dP^T may overwrite those columns.  The item's first dK overwrites the
-                // accumulator: the readout warps must have read the previous item's dK out of it.
-                if (!(ok = warp_wait(&bars->ds_full[b], ph2, bars, status))) break;
-                if (it == 0 && k > 0 && !(ok = warp_wait(&bars->dk_read, (k - 1) & 1, bars, status))) break;
-                tc_fence_after_sync();
-                if (leader) {
-#pragma unroll
-                    for (int ks = 0; ks < BM / 16; ++ks)
-                        mma_ts(tmem + C::COL_DK, tmem + C::COL_DP + ks * 8, sdesc_advance(q_mn, qoff + ks * 2048),
-                               idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
-                    tc_commit(&bars->q_empty[st]);
-                    if (nx < n) {
-                        issue_rows_dot<HD>(tmem + C::COL_DP, v_km, sdesc_advance(do_km, stn * C::Q_BYTES));
-                        tc_commit(&bars->dp_full);
-                    }
-                }
-                __syncwarp();
-                if (FUSED_DQ) {
-                    if (gi > 0 && !(ok = warp_wait(&bars->dq_empty, (gi - 1) & 1, bars, status))) break;
-                    tc_fence_after_sync();
-                    if (leader) {
-#pragma unroll
-                        for (int ks = 0; ks < BN / 16; ++ks)
-                            mma_ss(tmem + C::COL_DQ, sdesc_advance(k_mn, ks * 2048),
-                                   sdesc_advance(ds_mn, dsoff + ks * 2048), idesc_dq, ks > 0 ? 1u : 0u);
-                        tc_commit(&bars->dq_full);
-                        tc_commit(&bars->ds_empty[b]);
-                    }
-                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&mbars->full[st]);
+                    ++nm;
                 }
             }
-            if (!ok) break;
-            if (leader) tc_commit(&bars->done);   // every MMA of this item (K, V, the accumulators)
-            __syncwarp();
-            gt += n;
         }
-        if (leader) {
-            tc_commit(&bars->drain);
-            mbar_wait(&bars->drain, 0, nullptr);
-        }
-        __syncwarp();
     } else if (warp < 4) {
+        if (DROP) regs_increase<200>();
         // thread = key row r of the item's key tile (TMEM lane)
         const int r = warp * 32 + lane;
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
@@ -483,6 +557,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int i0 = (it0 + it) * BM;
                 const float *Ls = ld_s + st * 2 * BM;
                 const float *Ds = Ls + BM;
+                // dropout: keep bits of (row i0 + c, key) for the 64 columns, drawn ahead by the mask
+                // warps (their stages follow the same running tile count)
+                uint32_t km[2] = {0u, 0u};
+                if (DROP) {
+                    const uint32_t mst = gi % MSB;
+                    if (!(ok = warp_wait(&mbars->full[mst], (gi / MSB) & 1, bars, status))) break;
+                    const uint2 v = *reinterpret_cast<const uint2 *>(mask_s + (mst * BN + r) * 2);
+                    km[0] = v.x;
+                    km[1] = v.y;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&mbars->empty[mst]);
+                }
                 // S^T of this tile: one buffer (phase per tile) or two alternating (phase per pair)
                 const uint32_t t_s = tmem + lane_off + C::template col_s<FUSED_DQ>(gi);
                 if (!(ok = !TWO_S ? warp_wait(&bars->s_full[0], gi & 1, bars, status)
@@ -499,12 +585,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t cs2 = f2_pack(scale_log2, scale_log2);
                 const bool diag = key > i0;   // some (key > row) pairs in this tile
                 uint64_t pp[32];              // P pairs (fp32) kept for dS
-                // dropout: element (row i0 + c, key) has flat index (head*S + i0 + c)*S + key; its index times
-                // the golden ratio steps by S * golden per column.  Keep bits of the 64 columns in km.
-                uint32_t km[2] = {0u, 0u};
-                uint64_t drop_g = DROP ? (((uint64_t)head * S + (uint64_t)i0) * (uint64_t)S + (uint64_t)key) * kDropGolden
-                                       : 0ull;
-                const uint64_t drop_step = DROP ? (uint64_t)S * kDropGolden : 0ull;
                 {
                     uint32_t pk[32];
 #pragma unroll
@@ -522,10 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             pp[cc / 2] = f2_pack(p0, p1);
                             if (DROP) {
-                                const bool k0 = drop_keep(drop.seed, drop_g, drop.keep_thr);
-                                const bool k1 = drop_keep(drop.seed, drop_g + drop_step, drop.keep_thr);
-                                drop_g += 2 * drop_step;
-                                km[cc / 32] |= ((uint32_t)k0 << (cc % 32)) | ((uint32_t)k1 << (cc % 32 + 1));
+                                const bool k0 = (km[cc / 32] >> (cc % 32)) & 1u;
+                                const bool k1 = (km[cc / 32] >> (cc % 32 + 1)) & 1u;
                                 pk[cc / 2] = pack_bf16x2(k0 ? p0 * drop.inv_keep : 0.0f, k1 ? p1 * drop.inv_keep : 0.0f);
                             } else {
                                 pk[cc / 2] = pack_bf16x2(p0, p1);
@@ -697,15 +775,16 @@ int run(const BwdParams &p, cudaStream_t st)
     if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tq, p.q, HD, p.S, p.bh, BM);
     if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tdo, p.dout, HD, p.S, p.bh, BM);
     if (rc != XFA_OK) return rc;
-    static_assert(Cfg<HD>::SMEM <= 227 * 1024, "shared memory per CTA");
+    constexpr int smem = Cfg<HD, DROP>::SMEM;
+    static_assert(smem <= 227 * 1024, "shared memory per CTA");
     auto kern = tc_bwd_kernel<HD, FUSED_DQ, DROP>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<HD>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return XFA_ERR_CUDA_BASE + (int)e;
     const int nkt = (p.S + BN - 1) / BN;
     const unsigned grid = (unsigned)std::min(nkt * p.bh, device_sm_count());   // persistent: one CTA per SM
     unsigned *ctr = nullptr;
     if ((rc = next_item_counter(st, &ctr)) != XFA_OK) return rc;
-    kern<<<grid, kThreads, Cfg<HD>::SMEM, st>>>(tk, tv, tq, tdo, p.Lg, p.D, p.dq_acc, (__nv_bfloat16 *)p.dk,
+    kern<<<grid, DROP ? kThreadsDrop : kThreads, smem, st>>>(tk, tv, tq, tdo, p.Lg, p.D, p.dq_acc, (__nv_bfloat16 *)p.dk,
                                                  (__nv_bfloat16 *)p.dv, p.bh, p.S, p.S_pad, p.scale,
                                                  p.scale * 1.4426950408889634f, p.status, p.drop,
                                                  head_bundle(p.bh, p.S, HD, 2, kHeadBundle), ctr);

@@ -41,6 +41,14 @@ constexpr int BM = 128;               // query rows per tile (MMA M)
 constexpr int BN = 128;               // keys per tile (MMA N of S, K of P.V)
 constexpr int kThreads = 320;         // 10 warps
 constexpr int kWarpTma = 8, kWarpMma = 9;
+// With dropout: 16 warps.  Warps 12-15 draw the keep bits of every (row, key) of the coming key
+// tiles into shared memory (MS stages per tile), so the softmax warps only read them; warps 10-11
+// are idle.  Registers move from the TMA/MMA/idle warpgroup and the mask warpgroup to the softmax
+// warpgroups: 2 x 176 + 56 + 96 = 512 per lane of a warpgroup, the 65536 of a 512-thread launch.
+constexpr int kThreadsDrop = 512;
+constexpr int kWarpMask0 = 12;
+constexpr int MS = 2;                 // keep-bit stages per tile
+constexpr int kMaskBytes = 2 * MS * 128 * 16;   // [tile][stage][row] x 128 bits
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr int kHeadBundle = 8;              // heads scheduled together at long S (L2 reuse of K/V)
@@ -56,7 +64,9 @@ struct Cfg {
     static constexpr int OFF_K = 2 * TILE_BYTES;
     static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
     static constexpr int OFF_BAR = OFF_V + NS * TILE_BYTES;
-    static constexpr int SMEM = OFF_BAR + 512 + 1024;   // barriers + alignment slack
+    static constexpr int OFF_MASK = OFF_BAR + 512;      // keep bits (dropout only)
+    template <bool DROP>
+    static constexpr int smem() { return OFF_MASK + (DROP ? kMaskBytes : 0) + 1024; }   // + alignment slack
     // TMEM columns of S_t and O_t
     static __device__ __forceinline__ uint32_t col_s(int t) { return 128u * (uint32_t)t; }
     static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + (uint32_t)(HD * t); }
@@ -70,6 +80,8 @@ struct Bars {
     uint64_t p_full[2];   // P_t written to TMEM (one arrival per softmax warp)
     uint64_t o_full[2];   // O_t complete (commit after the last P.V)
     uint64_t drain;       // MMA drain at teardown
+    uint64_t mask_full[2][MS];   // keep bits of tile t written (one arrival per mask warp)
+    uint64_t mask_empty[2][MS];  // read by the softmax group of tile t (one arrival per warp)
     uint64_t item_full[2];   // work-item id posted by the TMA warp
     uint64_t item_empty[2];  // id read by the MMA warp and the eight softmax warps
     int item_id[2];          // the posted ids (-1: no more work)
@@ -146,7 +158,7 @@ __device__ __forceinline__ void load_scores_half(uint32_t tS, int h, bool diag, 
 
 // DROP: dropout on the probabilities that enter P.V (the row sums l keep every p).
 template <int HD, bool DROP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ O,
                   float *__restrict__ lse, int bh, int S, float scale_log2, int *status, const DropParams drop,
@@ -195,8 +207,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->drain, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->item_full[i], 1);
-            mbar_init(&bars->item_empty[i], 1 + BM / 32 * 2);   // MMA warp + eight softmax warps
+            // MMA warp + eight softmax warps (+ four mask warps)
+            mbar_init(&bars->item_empty[i], 1 + BM / 32 * 2 + (DROP ? 4 : 0));
         }
+        for (int t = 0; t < 2; ++t)
+            for (int s = 0; s < MS; ++s) {
+                mbar_init(&bars->mask_full[t][s], 4);
+                mbar_init(&bars->mask_empty[t][s], BM / 32);
+            }
         bars->abort = 0;
         fence_barrier_init();
     }
@@ -208,149 +226,204 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
+    uint32_t *mask_s = reinterpret_cast<uint32_t *>(smem + C::OFF_MASK);
 
-    if (warp == kWarpTma) {
-        if (lane == 0) {
-            prefetch_tensormap(&tm_q);
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-            uint32_t g = 0;                       // K/V tiles issued by this CTA
-            uint32_t last_k[3] = {0, 0, 0}, last_v[3] = {0, 0, 0};   // 1 + last tile issued per stage
-            int k = 0;                            // items whose Q was issued
+    // Roles by warpgroup (with dropout every warpgroup first resizes its registers, all four warps
+    // together): warps 8-11 the TMA and MMA warps (and two idle ones), 12-15 the keep-bit warps,
+    // 0-7 the softmax groups.
+    if (warp >= 8 && warp < 12) {
+        if (DROP) regs_decrease<56>();
+        if (warp == kWarpTma) {
+            if (lane == 0) {
+                prefetch_tensormap(&tm_q);
+                prefetch_tensormap(&tm_k);
+                prefetch_tensormap(&tm_v);
+                uint32_t g = 0;                       // K/V tiles issued by this CTA
+                uint32_t last_k[3] = {0, 0, 0}, last_v[3] = {0, 0, 0};   // 1 + last tile issued per stage
+                int k = 0;                            // items whose Q was issued
+                bool ok = true;
+                for (int kc = 0; ok; ++kc) {          // kc: items claimed, posted in ring entry kc & 1
+                    const int e = kc & 1;
+                    if (kc >= 2 && !(ok = mbar_wait_spin(&bars->item_empty[e], ((kc >> 1) + 1) & 1, &bars->abort))) break;
+                    int item = (int)atomicAdd(next_item, 1u);
+                    if (item >= n_items) item = -1;
+                    *reinterpret_cast<volatile int *>(&bars->item_id[e]) = item;
+                    mbar_arrive(&bars->item_full[e]);
+                    if (item < 0) break;
+                    int head, qb;
+                    item_coords(item, head, qb);
+                    const int q0 = qb * 2 * BM;
+                    const bool t1 = q0 + BM < S;
+                    const int nkv = t1 ? 2 * qb + 2 : 2 * qb + 1;
+                    // the Q buffers are free once the previous item's last S MMAs have read them
+                    if (k > 0 && !(ok = mbar_wait_spin(&bars->q_empty, (k - 1) & 1, &bars->abort))) break;
+                    mbar_arrive_expect_tx(&bars->q_full, (t1 ? 2 : 1) * C::TILE_BYTES);
+                    for (int s = 0; s < C::SUB; ++s) {
+                        tma_load_3d(smem + C::OFF_Q0 + s * C::SUB_BYTES, &tm_q, &bars->q_full, s * 64, q0, head);
+                        if (t1) tma_load_3d(smem + C::OFF_Q1 + s * C::SUB_BYTES, &tm_q, &bars->q_full, s * 64, q0 + BM, head);
+                    }
+                    ++k;
+                    for (int j = 0; j < nkv; ++j, ++g) {
+                        const int st = g % C::NS;
+                        const uint32_t ph = ((g / C::NS) + 1) & 1;   // parity of the release of the previous use
+                        if (g >= C::NS && !(ok = mbar_wait_spin(&bars->k_empty[st], ph, &bars->abort))) break;
+                        mbar_arrive_expect_tx(&bars->k_full[st], C::TILE_BYTES);
+                        for (int s = 0; s < C::SUB; ++s)
+                            tma_load_3d(smem + C::OFF_K + st * C::TILE_BYTES + s * C::SUB_BYTES, &tm_k, &bars->k_full[st],
+                                        s * 64, j * BN, head);
+                        last_k[st] = g + 1;
+                        if (g >= C::NS && !(ok = mbar_wait_spin(&bars->v_empty[st], ph, &bars->abort))) break;
+                        mbar_arrive_expect_tx(&bars->v_full[st], C::TILE_BYTES);
+                        for (int s = 0; s < C::SUB; ++s)
+                            tma_load_3d(smem + C::OFF_V + st * C::TILE_BYTES + s * C::SUB_BYTES, &tm_v, &bars->v_full[st],
+                                        s * 64, j * BN, head);
+                        last_v[st] = g + 1;
+                    }
+                }
+                if (!ok) fail(bars, status);
+                // Never leave the CTA with copies in flight: wait for the last load of Q and of each stage.
+                if (k > 0) mbar_wait_spin(&bars->q_full, (k - 1) & 1, nullptr);
+                for (int st = 0; st < C::NS; ++st) {
+                    if (last_k[st]) mbar_wait_spin(&bars->k_full[st], ((last_k[st] - 1) / C::NS) & 1, nullptr);
+                    if (last_v[st]) mbar_wait_spin(&bars->v_full[st], ((last_v[st] - 1) / C::NS) & 1, nullptr);
+                }
+            }
+        } else if (warp == kWarpMma) {
+            // The whole warp runs the issue loop (converged, so descriptors stay warp-uniform);
+            // one elected lane issues the tcgen05 instructions.
+            const bool leader = elect_one();
+            const uint64_t q_desc[2] = {sdesc_sw128(smem_u32(smem + C::OFF_Q0), 16, 1024),
+                                        sdesc_sw128(smem_u32(smem + C::OFF_Q1), 16, 1024)};
+            const uint64_t k_desc = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);
+            const uint64_t v_desc = sdesc_sw128(smem_u32(smem + C::OFF_V), C::SUB_BYTES, 1024);
+            uint32_t g = 0;                 // K/V tiles consumed by this CTA
+            uint32_t np[2] = {0, 0};        // P phases consumed per tile
+            int k = 0;                      // items started
             bool ok = true;
-            for (int kc = 0; ok; ++kc) {          // kc: items claimed, posted in ring entry kc & 1
-                const int e = kc & 1;
-                if (kc >= 2 && !(ok = mbar_wait_spin(&bars->item_empty[e], ((kc >> 1) + 1) & 1, &bars->abort))) break;
-                int item = (int)atomicAdd(next_item, 1u);
-                if (item >= n_items) item = -1;
-                *reinterpret_cast<volatile int *>(&bars->item_id[e]) = item;
-                mbar_arrive(&bars->item_full[e]);
+            for (; ok; ++k) {
+                const int item = take_item(bars, k, status, ok);
                 if (item < 0) break;
                 int head, qb;
                 item_coords(item, head, qb);
                 const int q0 = qb * 2 * BM;
                 const bool t1 = q0 + BM < S;
-                const int nkv = t1 ? 2 * qb + 2 : 2 * qb + 1;
-                // the Q buffers are free once the previous item's last S MMAs have read them
-                if (k > 0 && !(ok = mbar_wait_spin(&bars->q_empty, (k - 1) & 1, &bars->abort))) break;
-                mbar_arrive_expect_tx(&bars->q_full, (t1 ? 2 : 1) * C::TILE_BYTES);
-                for (int s = 0; s < C::SUB; ++s) {
-                    tma_load_3d(smem + C::OFF_Q0 + s * C::SUB_BYTES, &tm_q, &bars->q_full, s * 64, q0, head);
-                    if (t1) tma_load_3d(smem + C::OFF_Q1 + s * C::SUB_BYTES, &tm_q, &bars->q_full, s * 64, q0 + BM, head);
-                }
-                ++k;
-                for (int j = 0; j < nkv; ++j, ++g) {
-                    const int st = g % C::NS;
-                    const uint32_t ph = ((g / C::NS) + 1) & 1;   // parity of the release of the previous use
-                    if (g >= C::NS && !(ok = mbar_wait_spin(&bars->k_empty[st], ph, &bars->abort))) break;
-                    mbar_arrive_expect_tx(&bars->k_full[st], C::TILE_BYTES);
-                    for (int s = 0; s < C::SUB; ++s)
-                        tma_load_3d(smem + C::OFF_K + st * C::TILE_BYTES + s * C::SUB_BYTES, &tm_k, &bars->k_full[st],
-                                    s * 64, j * BN, head);
-                    last_k[st] = g + 1;
-                    if (g >= C::NS && !(ok = mbar_wait_spin(&bars->v_empty[st], ph, &bars->abort))) break;
-                    mbar_arrive_expect_tx(&bars->v_full[st], C::TILE_BYTES);
-                    for (int s = 0; s < C::SUB; ++s)
-                        tma_load_3d(smem + C::OFF_V + st * C::TILE_BYTES + s * C::SUB_BYTES, &tm_v, &bars->v_full[st],
-                                    s * 64, j * BN, head);
-                    last_v[st] = g + 1;
-                }
-            }
-            if (!ok) fail(bars, status);
-            // Never leave the CTA with copies in flight: wait for the last load of Q and of each stage.
-            if (k > 0) mbar_wait_spin(&bars->q_full, (k - 1) & 1, nullptr);
-            for (int st = 0; st < C::NS; ++st) {
-                if (last_k[st]) mbar_wait_spin(&bars->k_full[st], ((last_k[st] - 1) / C::NS) & 1, nullptr);
-                if (last_v[st]) mbar_wait_spin(&bars->v_full[st], ((last_v[st] - 1) / C::NS) & 1, nullptr);
-            }
-        }
-    } else if (warp == kWarpMma) {
-        // The whole warp runs the issue loop (converged, so descriptors stay warp-uniform);
-        // one elected lane issues the tcgen05 instructions.
-        const bool leader = elect_one();
-        const uint64_t q_desc[2] = {sdesc_sw128(smem_u32(smem + C::OFF_Q0), 16, 1024),
-                                    sdesc_sw128(smem_u32(smem + C::OFF_Q1), 16, 1024)};
-        const uint64_t k_desc = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);
-        const uint64_t v_desc = sdesc_sw128(smem_u32(smem + C::OFF_V), C::SUB_BYTES, 1024);
-        uint32_t g = 0;                 // K/V tiles consumed by this CTA
-        uint32_t np[2] = {0, 0};        // P phases consumed per tile
-        int k = 0;                      // items started
-        bool ok = true;
-        for (; ok; ++k) {
-            const int item = take_item(bars, k, status, ok);
-            if (item < 0) break;
-            int head, qb;
-            item_coords(item, head, qb);
-            const int q0 = qb * 2 * BM;
-            const bool t1 = q0 + BM < S;
-            const int n_t0 = 2 * qb + 1, n_t1 = t1 ? 2 * qb + 2 : 0;
-            const int nkv = t1 ? n_t1 : n_t0;
-            const int st0 = g % C::NS;
-            ok = warp_wait(&bars->q_full, k & 1, bars, status) &&
-                 warp_wait(&bars->k_full[st0], (g / C::NS) & 1, bars, status);
-            if (!ok) break;
-            tc_fence_after_sync();
-            if (leader) {
-                // S_0 of both tiles.  Each S buffer last held the previous item's final P, read by
-                // its last P.V issued before: the tensor pipe runs in order.
-                issue_qk<HD>(tmem + C::col_s(0), q_desc[0], sdesc_advance(k_desc, st0 * C::TILE_BYTES));
-                tc_commit(&bars->s_full[0]);
-                if (t1) {
-                    issue_qk<HD>(tmem + C::col_s(1), q_desc[1], sdesc_advance(k_desc, st0 * C::TILE_BYTES));
-                    tc_commit(&bars->s_full[1]);
-                }
-                tc_commit(&bars->k_empty[st0]);
-                if (nkv == 1) tc_commit(&bars->q_empty);   // no further S of this item reads Q
-            }
-            __syncwarp();
-            for (int j = 0; ok && j < nkv; ++j) {
-                const uint32_t gj = g + j, gn = gj + 1;
-                const int st = gj % C::NS, stn = gn % C::NS;
-                const uint32_t ph = (gj / C::NS) & 1, phn = (gn / C::NS) & 1;
-                bool v_ready = false, k_next_ready = false;
-                const int jn = j + 1;
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    const int nt = t == 0 ? n_t0 : n_t1;
-                    if (j >= nt) continue;
-                    ok = warp_wait(&bars->p_full[t], np[t] & 1, bars, status);
-                    ++np[t];
-                    if (ok && !v_ready) ok = v_ready = warp_wait(&bars->v_full[st], ph, bars, status);
-                    if (!ok) break;
-                    tc_fence_after_sync();
-                    if (leader) {
-                        issue_pv<HD>(tmem + C::col_o(t), tmem + C::col_s(t), sdesc_advance(v_desc, st * C::TILE_BYTES),
-                                     j > 0);
-                        if (j == nt - 1) tc_commit(&bars->o_full[t]);
+                const int n_t0 = 2 * qb + 1, n_t1 = t1 ? 2 * qb + 2 : 0;
+                const int nkv = t1 ? n_t1 : n_t0;
+                const int st0 = g % C::NS;
+                ok = warp_wait(&bars->q_full, k & 1, bars, status) &&
+                     warp_wait(&bars->k_full[st0], (g / C::NS) & 1, bars, status);
+                if (!ok) break;
+                tc_fence_after_sync();
+                if (leader) {
+                    // S_0 of both tiles.  Each S buffer last held the previous item's final P, read by
+                    // its last P.V issued before: the tensor pipe runs in order.
+                    issue_qk<HD>(tmem + C::col_s(0), q_desc[0], sdesc_advance(k_desc, st0 * C::TILE_BYTES));
+                    tc_commit(&bars->s_full[0]);
+                    if (t1) {
+                        issue_qk<HD>(tmem + C::col_s(1), q_desc[1], sdesc_advance(k_desc, st0 * C::TILE_BYTES));
+                        tc_commit(&bars->s_full[1]);
                     }
-                    __syncwarp();
-                    if (jn < nt) {
-                        if (!k_next_ready) ok = k_next_ready = warp_wait(&bars->k_full[stn], phn, bars, status);
+                    tc_commit(&bars->k_empty[st0]);
+                    if (nkv == 1) tc_commit(&bars->q_empty);   // no further S of this item reads Q
+                }
+                __syncwarp();
+                for (int j = 0; ok && j < nkv; ++j) {
+                    const uint32_t gj = g + j, gn = gj + 1;
+                    const int st = gj % C::NS, stn = gn % C::NS;
+                    const uint32_t ph = (gj / C::NS) & 1, phn = (gn / C::NS) & 1;
+                    bool v_ready = false, k_next_ready = false;
+                    const int jn = j + 1;
+    #pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const int nt = t == 0 ? n_t0 : n_t1;
+                        if (j >= nt) continue;
+                        ok = warp_wait(&bars->p_full[t], np[t] & 1, bars, status);
+                        ++np[t];
+                        if (ok && !v_ready) ok = v_ready = warp_wait(&bars->v_full[st], ph, bars, status);
                         if (!ok) break;
                         tc_fence_after_sync();
                         if (leader) {
-                            issue_qk<HD>(tmem + C::col_s(t), q_desc[t], sdesc_advance(k_desc, stn * C::TILE_BYTES));
-                            tc_commit(&bars->s_full[t]);
+                            issue_pv<HD>(tmem + C::col_o(t), tmem + C::col_s(t), sdesc_advance(v_desc, st * C::TILE_BYTES),
+                                         j > 0);
+                            if (j == nt - 1) tc_commit(&bars->o_full[t]);
                         }
                         __syncwarp();
+                        if (jn < nt) {
+                            if (!k_next_ready) ok = k_next_ready = warp_wait(&bars->k_full[stn], phn, bars, status);
+                            if (!ok) break;
+                            tc_fence_after_sync();
+                            if (leader) {
+                                issue_qk<HD>(tmem + C::col_s(t), q_desc[t], sdesc_advance(k_desc, stn * C::TILE_BYTES));
+                                tc_commit(&bars->s_full[t]);
+                            }
+                            __syncwarp();
+                        }
+                    }
+                    if (!ok) break;
+                    if (leader) {
+                        if (k_next_ready) tc_commit(&bars->k_empty[stn]);
+                        tc_commit(&bars->v_empty[st]);
+                        if (jn == nkv - 1) tc_commit(&bars->q_empty);   // the item's last S MMAs are issued
+                    }
+                    __syncwarp();
+                }
+                g += nkv;
+            }
+            if (leader) {
+                tc_commit(&bars->drain);
+                mbar_wait_spin(&bars->drain, 0, nullptr);
+            }
+            __syncwarp();
+        }
+    } else if (warp >= 12) {
+        if (DROP) {
+            regs_decrease<96>();
+            // keep bits (dropout): thread = row r of both tiles; for every key tile of the item, in
+            // the order the softmax groups consume them, the 128 decisions of the row's keys as
+            // four 32-bit words, element (row, key) drawn from its flat index (head*S + row)*S + key
+            const int r = (warp - kWarpMask0) * 32 + lane;
+            uint32_t nm[2] = {0u, 0u};   // stages filled per tile
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int item = take_item(bars, k, status, ok);
+                if (item < 0) break;
+                int head, qb;
+                item_coords(item, head, qb);
+                const int q0 = qb * 2 * BM;
+                const bool t1 = q0 + BM < S;
+                const int n_t0 = 2 * qb + 1, n_t1 = t1 ? 2 * qb + 2 : 0;
+                const int nkv = t1 ? n_t1 : n_t0;
+                for (int j = 0; ok && j < nkv; ++j) {
+#pragma unroll 1
+                    for (int t = 0; t < 2; ++t) {
+                        if (j >= (t == 0 ? n_t0 : n_t1)) continue;
+                        const uint32_t st = nm[t] % MS;
+                        if (nm[t] >= MS &&
+                            !(ok = warp_wait(&bars->mask_empty[t][st], ((nm[t] / MS) + 1) & 1, bars, status)))
+                            break;
+                        const uint64_t row = (uint64_t)(q0 + t * BM + r);
+                        uint64_t g = (((uint64_t)head * S + row) * (uint64_t)S + (uint64_t)(j * BN)) * kDropGolden;
+                        uint32_t w[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t bits = 0u;
+#pragma unroll 8
+                            for (int b = 0; b < 32; ++b) {
+                                bits |= (uint32_t)drop_keep(drop.seed, g, drop.keep_thr) << b;
+                                g += kDropGolden;
+                            }
+                            w[q] = bits;
+                        }
+                        *reinterpret_cast<uint4 *>(mask_s + ((t * MS + st) * BM + r) * 4) = make_uint4(w[0], w[1], w[2], w[3]);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars->mask_full[t][st]);
+                        ++nm[t];
                     }
                 }
-                if (!ok) break;
-                if (leader) {
-                    if (k_next_ready) tc_commit(&bars->k_empty[stn]);
-                    tc_commit(&bars->v_empty[st]);
-                    if (jn == nkv - 1) tc_commit(&bars->q_empty);   // the item's last S MMAs are issued
-                }
-                __syncwarp();
             }
-            g += nkv;
         }
-        if (leader) {
-            tc_commit(&bars->drain);
-            mbar_wait_spin(&bars->drain, 0, nullptr);
-        }
-        __syncwarp();
     } else {
+        if (DROP) regs_increase<176>();
         // softmax group of tile t; thread = query row
         const int t = warp / 4, wq = warp % 4;
         const int r = wq * 32 + lane;               // row within the tile == TMEM lane
@@ -358,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + lane_off + C::col_s(t);
         const uint32_t tO = tmem + lane_off + C::col_o(t);
         uint32_t ns = 0, no = 0;                    // S and O phases of this tile consumed
+        uint32_t nmask = 0;                         // keep-bit stages consumed (dropout)
         bool ok = true;
         for (int k = 0; ok; ++k) {
             const int item = take_item(bars, k, status, ok);
@@ -371,7 +445,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = q0 + t * BM + r;
             const int diag = 2 * qb + t;                // key tile that holds this tile's diagonal
             float m = -CUDART_INF_F, l = 0.0f;
-            const uint64_t drop_row_g = DROP ? ((uint64_t)head * S + (uint64_t)row) * (uint64_t)S * kDropGolden : 0ull;
             for (int j = 0; j < n_mine; ++j) {
                 if (!(ok = warp_wait(&bars->s_full[t], ns & 1, bars, status))) break;
                 ++ns;
@@ -412,6 +485,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     m = m_new;
                 }
+                // dropout: this row's keep bits of key tile j, drawn ahead by the mask warps
+                uint32_t kb[4] = {0u, 0u, 0u, 0u};
+                if (DROP) {
+                    const uint32_t st = nmask % MS;
+                    if (!(ok = warp_wait(&bars->mask_full[t][st], (nmask / MS) & 1, bars, status))) break;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(mask_s + ((t * MS + st) * BM + r) * 4);
+                    kb[0] = v.x;
+                    kb[1] = v.y;
+                    kb[2] = v.z;
+                    kb[3] = v.w;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->mask_empty[t][st]);
+                    ++nmask;
+                }
                 // p = 2^(s * scale * log2(e) - m): packed FFMA pairs + ex2; 4 packed partial row sums
                 const uint64_t c2 = f2_pack(scale_log2, scale_log2);
                 const uint64_t nm2 = f2_pack(-m, -m);
@@ -430,11 +517,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float p1 = ex2_approx(a.y);
                         l2[e & 3] = fadd2(l2[e & 3], f2_pack(p0, p1));
                         if (DROP) {
-                            // keys j*BN + c, c + 1 of this row: flat index (head*S + row)*S + key
-                            const uint64_t g0 = drop_row_g + (uint64_t)(j * BN + c) * kDropGolden;
-                            const float d0 = drop_keep(drop.seed, g0, drop.keep_thr) ? p0 * drop.inv_keep : 0.0f;
-                            const float d1 =
-                                drop_keep(drop.seed, g0 + kDropGolden, drop.keep_thr) ? p1 * drop.inv_keep : 0.0f;
+                            // keys j*BN + c, c + 1 of this row
+                            const float d0 = (kb[c >> 5] >> (c & 31)) & 1u ? p0 * drop.inv_keep : 0.0f;
+                            const float d1 = (kb[c >> 5] >> ((c + 1) & 31)) & 1u ? p1 * drop.inv_keep : 0.0f;
                             pk[e] = pack_bf16x2(d0, d1);
                         } else {
                             pk[e] = pack_bf16x2(p0, p1);
@@ -526,15 +611,16 @@ int run(const FwdParams &p, cudaStream_t st)
     if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tk, p.k, HD, p.S, p.bh, BN);
     if (rc == XFA_OK) rc = encode_tmap_bf16_3d(&tv, p.v, HD, p.S, p.bh, BN);
     if (rc != XFA_OK) return rc;
-    static_assert(Cfg<HD>::SMEM <= 227 * 1024, "shared memory per CTA");
+    constexpr int smem = Cfg<HD>::template smem<DROP>();
+    static_assert(smem <= 227 * 1024, "shared memory per CTA");
     auto kern = tc_fwd_kernel<HD, DROP>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<HD>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return XFA_ERR_CUDA_BASE + (int)e;
     const int nqb = (p.S + 2 * BM - 1) / (2 * BM);
     const unsigned grid = (unsigned)std::min(nqb * p.bh, device_sm_count());   // persistent: one CTA per SM
     unsigned *ctr = nullptr;
     if ((rc = next_item_counter(st, &ctr)) != XFA_OK) return rc;
-    kern<<<grid, kThreads, Cfg<HD>::SMEM, st>>>(tq, tk, tv, (__nv_bfloat16 *)p.out, p.lse, p.bh, p.S,
+    kern<<<grid, DROP ? kThreadsDrop : kThreads, smem, st>>>(tq, tk, tv, (__nv_bfloat16 *)p.out, p.lse, p.bh, p.S,
                                                  p.scale * 1.4426950408889634f, p.status, p.drop,
                                                  head_bundle(p.bh, p.S, HD, 2, kHeadBundle), ctr);
     e = cudaGetLastError();
