@@ -54,13 +54,16 @@ template <int HD, bool DROP>
 constexpr int ring_depth() { return HD == 128 ? (DROP ? 2 : 3) : 4; }
 constexpr int kThreads = 320;
 constexpr int kWarpTma = 8, kWarpMma = 9;
-// With dropout: 16 warps.  Warps 12-15 draw the keep bits of every (key, query row) of the
-// coming query tiles into shared memory (MSB stages), so the key-row warps only read them; warps
-// 10-11 are idle.  Registers: the key-row warpgroup grows to 200, the TMA/MMA/idle warpgroup
-// shrinks to 56 and the mask warpgroup to 96, the readout warpgroup keeps the 128 of a 512-thread
-// launch (200 + 128 + 56 + 96 <= 512 per lane of a warpgroup).
-constexpr int kThreadsDrop = 512;
+// With dropout: 20 warps.  Warps 12-19 (two warpgroups, two warps per SM sub-partition: the draw
+// is bound by the integer multiplier, which one warp per sub-partition does not keep busy) draw
+// the keep bits of every (key, query row) of the coming query tiles into shared memory (MSB
+// stages), so the key-row warps only read them; warps 10-11 are idle.  A 640-thread launch gets 96
+// registers a thread: the key-row warpgroup grows to 184 and the readout warpgroup to 128, the
+// TMA/MMA/idle warpgroup and the mask warpgroups shrink to 56 (184 + 128 + 56 + 2 x 56 = 480 per
+// lane of a warpgroup, 96 x 5).
+constexpr int kMaskWarps = 8;
 constexpr int kWarpMask0 = 12;
+constexpr int kThreadsDrop = (kWarpMask0 + kMaskWarps) * 32;
 constexpr int MSB = 4;   // keep-bit stages (query tiles)
 
 struct MaskBars {
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
             mbar_init(&bars->ds_empty[b], 1);
             mbar_init(&bars->item_full[b], 1);
             // MMA warp, four key warps, four readout warps (+ four mask warps)
-            mbar_init(&bars->item_empty[b], 9 + (DROP ? 4 : 0));
+            mbar_init(&bars->item_empty[b], 9 + (DROP ? kMaskWarps : 0));
         }
         mbar_init(&bars->s_full[0], 1);
         mbar_init(&bars->s_full[1], 1);
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
         if (DROP) {
             MaskBars *mb = reinterpret_cast<MaskBars *>(smem + C::OFF_MBAR);
             for (int s = 0; s < MSB; ++s) {
-                mbar_init(&mb->full[s], 4);
+                mbar_init(&mb->full[s], kMaskWarps);
                 mbar_init(&mb->empty[s], 4);
             }
         }
@@ -478,11 +481,13 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
         }
     } else if (warp >= 12) {
         if (DROP) {
-            regs_decrease<96>();
-            // keep bits (dropout): thread = key r of the item's key tile; for every query tile, in
-            // the order the key-row warps consume them, the 64 decisions of (row i0 + c, key) as two
-            // 32-bit words, element drawn from its flat index (head*S + i0 + c)*S + key
-            const int r = (warp - kWarpMask0) * 32 + lane;
+            regs_decrease<56>();
+            // keep bits (dropout): thread = key r of the item's key tile, half m of the query rows;
+            // for every query tile, in the order the key-row warps consume them, the 32 decisions of
+            // (row i0 + 32m + c, key) as one 32-bit word, element drawn from its flat index
+            // (head*S + i0 + 32m + c)*S + key
+            const int mw = warp - kWarpMask0;
+            const int r = (mw % 4) * 32 + lane, m = mw / 4;
             uint32_t *mask_w = reinterpret_cast<uint32_t *>(smem + C::OFF_MASK);
             uint32_t nm = 0;   // stages filled
             bool ok = true;
@@ -495,20 +500,15 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                 for (int it = 0; it < w.n; ++it) {
                     const uint32_t st = nm % MSB;
                     if (nm >= MSB && !(ok = warp_wait(&mbars->empty[st], ((nm / MSB) + 1) & 1, bars, status))) break;
-                    const uint64_t i0 = (uint64_t)((w.it0 + it) * BM);
+                    const uint64_t i0 = (uint64_t)((w.it0 + it) * BM + 32 * m);
                     uint64_t g = (((uint64_t)w.head * S + i0) * (uint64_t)S + key) * kDropGolden;
-                    uint32_t km[2];
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        uint32_t bits = 0u;
-#pragma unroll 8
-                        for (int b = 0; b < 32; ++b) {
-                            bits |= (uint32_t)drop_keep(drop.seed, g, drop.keep_thr) << b;
-                            g += step;
-                        }
-                        km[q] = bits;
+                    uint32_t bits = 0u;
+#pragma unroll 4
+                    for (int b = 0; b < 32; ++b) {
+                        bits |= (uint32_t)drop_keep(drop.seed, g, drop.keep_thr) << b;
+                        g += step;
                     }
-                    *reinterpret_cast<uint2 *>(mask_w + (st * BN + r) * 2) = make_uint2(km[0], km[1]);
+                    mask_w[(st * BN + r) * 2 + m] = bits;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&mbars->full[st]);
                     ++nm;
@@ -516,7 +516,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
             }
         }
     } else if (warp < 4) {
-        if (DROP) regs_increase<200>();
+        if (DROP) regs_increase<184>();
         // thread = key row r of the item's key tile (TMEM lane)
         const int r = warp * 32 + lane;
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
@@ -673,6 +673,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
             gt += n;
         }
     } else if (warp < 8) {
+        if (DROP) regs_increase<128>();
         // dQ readout: thread = hd index d (TMEM lane of dQ^T); then the item's dK rows (thread = key)
         const int wq = warp - 4;
         const int d = wq * 32 + lane;

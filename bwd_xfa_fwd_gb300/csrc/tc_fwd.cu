@@ -41,12 +41,15 @@ constexpr int BM = 128;               // query rows per tile (MMA M)
 constexpr int BN = 128;               // keys per tile (MMA N of S, K of P.V)
 constexpr int kThreads = 320;         // 10 warps
 constexpr int kWarpTma = 8, kWarpMma = 9;
-// With dropout: 16 warps.  Warps 12-15 draw the keep bits of every (row, key) of the coming key
-// tiles into shared memory (MS stages per tile), so the softmax warps only read them; warps 10-11
-// are idle.  Registers move from the TMA/MMA/idle warpgroup and the mask warpgroup to the softmax
-// warpgroups: 2 x 176 + 56 + 96 = 512 per lane of a warpgroup, the 65536 of a 512-thread launch.
-constexpr int kThreadsDrop = 512;
+// With dropout: 20 warps.  Warps 12-19 (two warpgroups, two warps per SM sub-partition: the draw
+// is bound by the integer multiplier, which one warp per sub-partition does not keep busy) draw
+// the keep bits of every (row, key) of the coming key tiles into shared memory (MS stages per
+// tile), so the softmax warps only read them; warps 10-11 are idle.  A 640-thread launch gets 96
+// registers a thread; they move from the TMA/MMA/idle warpgroup and the mask warpgroups to the
+// softmax warpgroups: 2 x 152 + 56 + 2 x 56 = 480 per lane of a warpgroup, 96 x 5.
+constexpr int kMaskWarps = 8;
 constexpr int kWarpMask0 = 12;
+constexpr int kThreadsDrop = (kWarpMask0 + kMaskWarps) * 32;
 constexpr int MS = 2;                 // keep-bit stages per tile
 constexpr int kMaskBytes = 2 * MS * 128 * 16;   // [tile][stage][row] x 128 bits
 constexpr float kLn2 = 0.6931471805599453f;
@@ -208,11 +211,11 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->item_full[i], 1);
             // MMA warp + eight softmax warps (+ four mask warps)
-            mbar_init(&bars->item_empty[i], 1 + BM / 32 * 2 + (DROP ? 4 : 0));
+            mbar_init(&bars->item_empty[i], 1 + BM / 32 * 2 + (DROP ? kMaskWarps : 0));
         }
         for (int t = 0; t < 2; ++t)
             for (int s = 0; s < MS; ++s) {
-                mbar_init(&bars->mask_full[t][s], 4);
+                mbar_init(&bars->mask_full[t][s], kMaskWarps);
                 mbar_init(&bars->mask_empty[t][s], BM / 32);
             }
         bars->abort = 0;
@@ -377,11 +380,13 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
         }
     } else if (warp >= 12) {
         if (DROP) {
-            regs_decrease<96>();
-            // keep bits (dropout): thread = row r of both tiles; for every key tile of the item, in
-            // the order the softmax groups consume them, the 128 decisions of the row's keys as
-            // four 32-bit words, element (row, key) drawn from its flat index (head*S + row)*S + key
-            const int r = (warp - kWarpMask0) * 32 + lane;
+            regs_decrease<56>();
+            // keep bits (dropout): thread = row r of both tiles, half m of the keys; for every key
+            // tile of the item, in the order the softmax groups consume them, the 64 decisions of
+            // the row's keys 64m..64m+63 as two 32-bit words, element (row, key) drawn from its flat
+            // index (head*S + row)*S + key
+            const int mw = warp - kWarpMask0;
+            const int r = (mw % 4) * 32 + lane, m = mw / 4;
             uint32_t nm[2] = {0u, 0u};   // stages filled per tile
             bool ok = true;
             for (int k = 0; ok; ++k) {
@@ -402,19 +407,19 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                             !(ok = warp_wait(&bars->mask_empty[t][st], ((nm[t] / MS) + 1) & 1, bars, status)))
                             break;
                         const uint64_t row = (uint64_t)(q0 + t * BM + r);
-                        uint64_t g = (((uint64_t)head * S + row) * (uint64_t)S + (uint64_t)(j * BN)) * kDropGolden;
-                        uint32_t w[4];
+                        uint64_t g = (((uint64_t)head * S + row) * (uint64_t)S + (uint64_t)(j * BN + 64 * m)) * kDropGolden;
+                        uint32_t w[2];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
+                        for (int q = 0; q < 2; ++q) {
                             uint32_t bits = 0u;
-#pragma unroll 8
+#pragma unroll 4
                             for (int b = 0; b < 32; ++b) {
                                 bits |= (uint32_t)drop_keep(drop.seed, g, drop.keep_thr) << b;
                                 g += kDropGolden;
                             }
                             w[q] = bits;
                         }
-                        *reinterpret_cast<uint4 *>(mask_s + ((t * MS + st) * BM + r) * 4) = make_uint4(w[0], w[1], w[2], w[3]);
+                        *reinterpret_cast<uint2 *>(mask_s + ((t * MS + st) * BM + r) * 4 + 2 * m) = make_uint2(w[0], w[1]);
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&bars->mask_full[t][st]);
                         ++nm[t];
@@ -423,7 +428,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
             }
         }
     } else {
-        if (DROP) regs_increase<176>();
+        if (DROP) regs_increase<152>();
         // softmax group of tile t; thread = query row
         const int t = warp / 4, wq = warp % 4;
         const int r = wq * 32 + lane;               // row within the tile == TMEM lane
