@@ -56,14 +56,15 @@ KERNEL_SOURCES = {
 
 
 def source_hash(name):
-    """Hash of the code of a kernel's sources: // comments and blank lines are left out, so an
-    edit of the comments does not void a recorded capture, any edit of the code does."""
+    """Hash of the code of a kernel's sources: // comments, blank lines and indentation are left
+    out, so an edit of the comments or the layout does not void a recorded capture, any edit of
+    the code does."""
     import hashlib
     import re
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[name]:
         with open(os.path.join(ROOT, rel)) as f:
-            code = [re.sub(r"//.*$", "", line).rstrip() for line in f]
+            code = [re.sub(r"//.*$", "", line).strip() for line in f]
         h.update("\n".join(line for line in code if line).encode())
     return h.hexdigest()[:16]
 

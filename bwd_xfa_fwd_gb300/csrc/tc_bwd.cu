@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                     if (!(ok = warp_wait(&bars->p_full, gi & 1, bars, status))) break;
                     tc_fence_after_sync();
                     if (leader) {
-    #pragma unroll
+#pragma unroll
                         for (int ks = 0; ks < BM / 16; ++ks)
                             mma_ts(tmem + C::COL_DV, tmem + C::template col_s<FUSED_DQ>(gi) + ks * 8,
                                    sdesc_advance(do_mn, qoff + ks * 2048), idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                     if (it == 0 && k > 0 && !(ok = warp_wait(&bars->dk_read, (k - 1) & 1, bars, status))) break;
                     tc_fence_after_sync();
                     if (leader) {
-    #pragma unroll
+#pragma unroll
                         for (int ks = 0; ks < BM / 16; ++ks)
                             mma_ts(tmem + C::COL_DK, tmem + C::COL_DP + ks * 8, sdesc_advance(q_mn, qoff + ks * 2048),
                                    idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                         if (gi > 0 && !(ok = warp_wait(&bars->dq_empty, (gi - 1) & 1, bars, status))) break;
                         tc_fence_after_sync();
                         if (leader) {
-    #pragma unroll
+#pragma unroll
                             for (int ks = 0; ks < BN / 16; ++ks)
                                 mma_ss(tmem + C::COL_DQ, sdesc_advance(k_mn, ks * 2048),
                                        sdesc_advance(ds_mn, dsoff + ks * 2048), idesc_dq, ks > 0 ? 1u : 0u);

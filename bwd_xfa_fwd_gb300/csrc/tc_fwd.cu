@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                     const uint32_t ph = (gj / C::NS) & 1, phn = (gn / C::NS) & 1;
                     bool v_ready = false, k_next_ready = false;
                     const int jn = j + 1;
-    #pragma unroll
+#pragma unroll
                     for (int t = 0; t < 2; ++t) {
                         const int nt = t == 0 ? n_t0 : n_t1;
                         if (j >= nt) continue;
