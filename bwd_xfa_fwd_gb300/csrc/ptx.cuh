@@ -338,6 +338,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r)
         : "r"(taddr));
 }
 
+// Load 32 consecutive fp32 columns of this warp's 32 TMEM lanes and reduce them: returns the
+// maximum of this thread's 32 values (the loaded values themselves are not kept).  The result is
+// valid after tmem_wait_ld().
+__device__ __forceinline__ float tmem_ld32_max(uint32_t taddr)
+{
+    uint32_t r[32];
+    float mx;
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+        : XFA_R8(0), XFA_R8(8), XFA_R8(16), XFA_R8(24), "=f"(mx)
+        : "r"(taddr));
+    return mx;
+}
+
 __device__ __forceinline__ void tmem_wait_ld()
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -348,6 +364,11 @@ __device__ __forceinline__ void tmem_wait_ld()
 __device__ __forceinline__ void reg_fence32(uint32_t *r)
 {
     asm volatile("" : XFA_F8(0), XFA_F8(8), XFA_F8(16), XFA_F8(24));
+}
+
+__device__ __forceinline__ void reg_fence_f4(float &a, float &b, float &c, float &d)
+{
+    asm volatile("" : "+f"(a), "+f"(b), "+f"(c), "+f"(d));
 }
 
 // Store 32 / 16 consecutive 32-bit columns of this warp's 32 TMEM lanes.

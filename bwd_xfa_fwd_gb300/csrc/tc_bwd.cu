@@ -114,6 +114,10 @@ constexpr int kMaxRing = 4;
 struct Bars {
     uint64_t kv_full;
     uint64_t q_full[kMaxRing], q_empty[kMaxRing];
+    // ds_full[b]: dS of a tile written (key warps) and, with the fused dQ at hd = 64, the previous
+    // tile's dQ^T read out of TMEM (readout warps) -- one barrier for the MMA warp to wait on before
+    // the tile's dK, next dP^T and dQ^T.  At hd = 128 the readout signals dq_empty instead: there
+    // its staging is long enough that tying dK to it would hold up the whole chain.
     uint64_t s_full[2], p_full, ds_full[2], ds_empty[2];
     uint64_t kt_full, dp_full, dq_full, dq_empty, done, drain;
     uint64_t dk_read;                      // the readout warps have read the item's dK out of TMEM
@@ -259,7 +263,8 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
             mbar_init(&bars->q_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&bars->ds_full[b], 4);   // one arrival per key warp
+            // one arrival per key warp (+ one per dQ readout warp at hd = 64)
+            mbar_init(&bars->ds_full[b], 4 + (FUSED_DQ && HD == 64 ? HD / 32 : 0));
             mbar_init(&bars->ds_empty[b], 1);
             mbar_init(&bars->item_full[b], 1);
             // MMA warp, four key warps, four readout warps (+ four mask warps)
@@ -271,7 +276,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
         mbar_init(&bars->kt_full, 4);
         mbar_init(&bars->dp_full, 1);
         mbar_init(&bars->dq_full, 1);
-        mbar_init(&bars->dq_empty, HD / 32);   // one arrival per readout warp
+        mbar_init(&bars->dq_empty, HD / 32);   // one arrival per readout warp (hd = 128)
         mbar_init(&bars->done, 1);
         mbar_init(&bars->dk_read, 4);         // one arrival per readout warp
         mbar_init(&bars->drain, 1);
@@ -439,6 +444,8 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                     // dS^T is in TMEM (first columns of dP^T) and in smem: dK first (reads the TMEM copy),
                     // then the next dP^T may overwrite those columns.  The item's first dK overwrites the
                     // accumulator: the readout warps must have read the previous item's dK out of it.
+                    // With the fused dQ at hd = 64 the same barrier also says that the readout warps have
+                    // read the previous tile's dQ^T out of TMEM, so this tile's dQ^T may overwrite it.
                     if (!(ok = warp_wait(&bars->ds_full[b], ph2, bars, status))) break;
                     if (it == 0 && k > 0 && !(ok = warp_wait(&bars->dk_read, (k - 1) & 1, bars, status))) break;
                     tc_fence_after_sync();
@@ -455,7 +462,8 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                     }
                     __syncwarp();
                     if (FUSED_DQ) {
-                        if (gi > 0 && !(ok = warp_wait(&bars->dq_empty, (gi - 1) & 1, bars, status))) break;
+                        if (HD == 128 && gi > 0 && !(ok = warp_wait(&bars->dq_empty, (gi - 1) & 1, bars, status)))
+                            break;
                         tc_fence_after_sync();
                         if (leader) {
 #pragma unroll
@@ -463,7 +471,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                                 mma_ss(tmem + C::COL_DQ, sdesc_advance(k_mn, ks * 2048),
                                        sdesc_advance(ds_mn, dsoff + ks * 2048), idesc_dq, ks > 0 ? 1u : 0u);
                             tc_commit(&bars->dq_full);
-                            tc_commit(&bars->ds_empty[b]);
+                            if (HD == 128) tc_commit(&bars->ds_empty[b]);
                         }
                         __syncwarp();
                     }
@@ -619,7 +627,12 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
 
                 if (!(ok = warp_wait(&bars->dp_full, gi & 1, bars, status))) break;
                 tc_fence_after_sync();
-                if (FUSED_DQ && gi >= 2 && !(ok = warp_wait(&bars->ds_empty[b], ph2 ^ 1, bars, status))) break;
+                // dS buffer b was last read by the dQ^T MMA of tile gi - 2, which the MMA warp issued
+                // before this tile's S^T: the S^T commit waited for above tracks it, so the buffer is
+                // free.  At hd = 128 the key warps still wait for that MMA's own commit (measured:
+                // dropping the wait there made the kernel 4 % slower)
+                if (FUSED_DQ && HD == 128 && gi >= 2 && !(ok = warp_wait(&bars->ds_empty[b], ph2 ^ 1, bars, status)))
+                    break;
                 uint8_t *dsrow = smem + C::OFF_DS + b * C::DS_BYTES + r * 128;
                 // dS = P (dP - D) scale on packed pairs
                 const uint64_t sc2 = f2_pack(scale, scale);
@@ -680,6 +693,9 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         uint32_t gt = 0;   // query tiles of earlier items
         bool ok = true;
+        // at hd = 64 the MMA warp waits for this warp on ds_full before every dQ^T; tile 0 has no
+        // predecessor
+        if (FUSED_DQ && HD == 64 && d < HD && lane == 0) mbar_arrive(&bars->ds_full[0]);
         for (int k = 0; ok; ++k) {
             const int item = take_item(bars, k, status, ok);
             if (item < 0) break;
@@ -698,7 +714,8 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                     reg_fence32(g + 32);
                     tc_fence_before_sync();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars->dq_empty);
+                    // dQ^T of tile gi is out of TMEM: the next tile's dQ^T may be issued
+                    if (lane == 0) mbar_arrive(HD == 64 ? &bars->ds_full[(gi + 1) & 1] : &bars->dq_empty);
                     const int i0 = (w.it0 + it) * BM;
                     const int rows = min(BM, S - i0);
                     // the staging tile is free once the previous bulk reduce has read it

@@ -459,15 +459,25 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                 // chains of 3-input maxima.
                 const bool on_diag = j == diag;
                 float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+                if (HD == 64 && !on_diag) {
+                    // no masked keys: TMEM loads that reduce while loading (max of 32 columns each).
+                    // At hd = 64, where the softmax sets the pace, this is 4 % faster; at hd = 128 it
+                    // measured no better than the plain loads, which are kept there.
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t sh[64];
-                    load_scores_half(tS, h, on_diag, r, sh);
+                    for (int q = 0; q < 4; ++q) mx4[q] = tmem_ld32_max(tS + 32 * q);
+                    tmem_wait_ld();
+                    reg_fence_f4(mx4[0], mx4[1], mx4[2], mx4[3]);
+                } else {
 #pragma unroll
-                    for (int c = 0; c < 64; c += 8)
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t sh[64];
+                        load_scores_half(tS, h, on_diag, r, sh);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            mx4[e] = fmax3(mx4[e], __uint_as_float(sh[c + 2 * e]), __uint_as_float(sh[c + 2 * e + 1]));
+                        for (int c = 0; c < 64; c += 8)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                mx4[e] = fmax3(mx4[e], __uint_as_float(sh[c + 2 * e]), __uint_as_float(sh[c + 2 * e + 1]));
+                    }
                 }
                 const float mx = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
                 const float m_new = fmaxf(m, mx * scale_log2);   // scale > 0: max commutes with the scaling
