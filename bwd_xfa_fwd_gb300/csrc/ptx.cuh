@@ -71,22 +71,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Non-blocking test for the completion of the phase with parity `parity` (acquire on success).
-// Its result is only read where it is needed, so the shared-memory round trip of the test can
-// overlap the work issued in between.
-__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // As mbar_try_wait, but the thread may stay suspended in the instruction until the phase
 // completes or `hint_ns` has passed (the suspend-time hint), instead of the system's shorter
 // default -- fewer polls of the barrier word in shared memory.
