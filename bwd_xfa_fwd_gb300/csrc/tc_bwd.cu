@@ -637,12 +637,17 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                 // dS = P (dP - D) scale on packed pairs
                 const uint64_t sc2 = f2_pack(scale, scale);
                 const uint64_t m1 = f2_pack(-1.0f, -1.0f);
+                // all 64 dP columns with one tcgen05.wait::ld (each wait waits for every load in flight;
+                // one wait instead of two per tile measured 1-5 % faster)
+                uint32_t dpa[64];
+                tmem_ld32(tmem + lane_off + C::COL_DP, dpa);
+                tmem_ld32(tmem + lane_off + C::COL_DP + 32, dpa + 32);
+                tmem_wait_ld();
+                reg_fence32(dpa);
+                reg_fence32(dpa + 32);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    uint32_t dp[32];
-                    tmem_ld32(tmem + lane_off + C::COL_DP + 32 * h, dp);
-                    tmem_wait_ld();
-                    reg_fence32(dp);
+                    const uint32_t *dp = dpa + 32 * h;
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
