@@ -343,7 +343,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r)
 // valid after tmem_wait_ld().
 __device__ __forceinline__ float tmem_ld32_max(uint32_t taddr)
 {
-    uint32_t r[32];
+    [[maybe_unused]] uint32_t r[32];
     float mx;
     asm volatile(
         "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "

@@ -133,6 +133,13 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint6
     }
 }
 
+// TMEM column (from the start of S_t) of the packed P of keys 16ks .. 16ks + 15.  hd = 128: keys 0-63
+// in columns 0-31, keys 64-127 in columns 96-127 (the softmax writes the second half's P from the
+// scores it still holds from the maximum pass, over score columns of that half, before it re-reads
+// the first half); hd = 64: columns 0-63 in order.
+template <int HD>
+__host__ __device__ constexpr uint32_t p_col(int ks) { return HD == 128 && ks >= 4 ? 96 + 8 * (ks - 4) : 8 * ks; }
+
 // O += P V: P (bf16) from TMEM, V [keys][hd] as an MN-major B operand; 16 keys = 2048 bytes.
 template <int HD>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, bool accumulate)
@@ -140,7 +147,7 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
     constexpr uint32_t idesc = idesc_bf16(BM, HD, false, true);
 #pragma unroll
     for (int ks = 0; ks < BN / 16; ++ks)
-        mma_ts(o_tmem, p_tmem + ks * 8, sdesc_advance(v_desc, ks * 2048), idesc, (accumulate || ks > 0) ? 1u : 0u);
+        mma_ts(o_tmem, p_tmem + p_col<HD>(ks), sdesc_advance(v_desc, ks * 2048), idesc, (accumulate || ks > 0) ? 1u : 0u);
 }
 
 // Raw scores of columns 64h..64h+63 of this thread's row of S_t (TMEM lane); on the
@@ -459,6 +466,8 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                 // chains of 3-input maxima.
                 const bool on_diag = j == diag;
                 float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+                // hd = 128: the second half's scores (s1) stay in registers for the exponential pass
+                uint32_t s0[64], s1[64];
                 if (HD == 64 && !on_diag) {
                     // no masked keys: TMEM loads that reduce while loading (max of 32 columns each).
                     // At hd = 64, where the softmax sets the pace, this is 4 % faster; at hd = 128 it
@@ -470,7 +479,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                 } else {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        uint32_t sh[64];
+                        uint32_t *sh = h == 0 ? s0 : s1;
                         load_scores_half(tS, h, on_diag, r, sh);
 #pragma unroll
                         for (int c = 0; c < 64; c += 8)
@@ -518,11 +527,14 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                 const uint64_t c2 = f2_pack(scale_log2, scale_log2);
                 const uint64_t nm2 = f2_pack(-m, -m);
                 uint64_t l2[4] = {0ull, 0ull, 0ull, 0ull};
-                // pass 2: the exponentials, half a row at a time (the scores read again)
+                // pass 2: the exponentials, half a row at a time.  hd = 128: the second half first, from
+                // the registers of the maximum pass (its P over its own score columns 96-127), then the
+                // first half read again (P over columns 0-31); hd = 64: both halves read again, in order.
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t sh[64];
-                    load_scores_half(tS, h, on_diag, r, sh);
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int h = HD == 128 ? 1 - hh : hh;
+                    uint32_t *sh = HD == 128 && h == 1 ? s1 : s0;
+                    if (!(HD == 128 && h == 1)) load_scores_half(tS, h, on_diag, r, sh);
                     uint32_t pk[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
@@ -540,7 +552,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                             pk[e] = pack_bf16x2(p0, p1);
                         }
                     }
-                    tmem_st32(tS + 32 * h, pk);
+                    tmem_st32(tS + p_col<HD>(4 * h), pk);
                 }
                 {
                     const float2 a = f2_unpack(fadd2(fadd2(l2[0], l2[1]), fadd2(l2[2], l2[3])));
