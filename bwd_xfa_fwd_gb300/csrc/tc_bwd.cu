@@ -107,6 +107,17 @@ struct Cfg {
     {
         return two_s<FUSED_DQ>() && (i & 1) ? (FUSED_DQ ? COL_S2 : COL_DQ) : COL_S;
     }
+    // dP^T buffers: with the fused dQ at hd = 64 there is room for a second one past the second
+    // S^T, and tiles alternate between the two, so the next tile's dP^T is issued before this
+    // tile's dK (which reads dS^T out of this tile's dP^T columns).
+    static constexpr uint32_t COL_DP2 = COL_S2 + 64;
+    template <bool FUSED_DQ>
+    static __host__ __device__ constexpr bool two_dp() { return FUSED_DQ && HD == 64 && COL_DP2 + 64 <= TMEM_COLS; }
+    template <bool FUSED_DQ>
+    static __device__ __forceinline__ uint32_t col_dp(uint32_t i)
+    {
+        return two_dp<FUSED_DQ>() && (i & 1) ? COL_DP2 : COL_DP;
+    }
 };
 
 constexpr int kMaxRing = 4;
@@ -119,7 +130,7 @@ struct Bars {
     // the tile's dK, next dP^T and dQ^T.  At hd = 128 the readout signals dq_empty instead: there
     // its staging is long enough that tying dK to it would hold up the whole chain.
     uint64_t s_full[2], p_full, ds_full[2], ds_empty[2];
-    uint64_t kt_full, dp_full, dq_full, dq_empty, done, drain;
+    uint64_t kt_full, dp_full[2], dq_full, dq_empty, done, drain;
     uint64_t dk_read;                      // the readout warps have read the item's dK out of TMEM
     uint64_t item_full[2], item_empty[2];  // work-item ids posted by the TMA warp, read by the others
     int item_id[2];                        // the posted ids (-1: no more work)
@@ -221,6 +232,8 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     using C = Cfg<HD, DROP>;
     constexpr int NSQ = C::NSQ;
     constexpr bool TWO_S = C::template two_s<FUSED_DQ>();
+    constexpr bool TWO_DP = C::template two_dp<FUSED_DQ>();
+    static_assert(!TWO_DP || TWO_S, "the early dP^T relies on the early S^T's wait for the query stage");
     static_assert(NSQ <= kMaxRing && sizeof(Bars) <= 256, "barrier block");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -274,7 +287,8 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
         mbar_init(&bars->s_full[1], 1);
         mbar_init(&bars->p_full, 4);
         mbar_init(&bars->kt_full, 4);
-        mbar_init(&bars->dp_full, 1);
+        mbar_init(&bars->dp_full[0], 1);
+        mbar_init(&bars->dp_full[1], 1);
         mbar_init(&bars->dq_full, 1);
         mbar_init(&bars->dq_empty, HD / 32);   // one arrival per readout warp (hd = 128)
         mbar_init(&bars->done, 1);
@@ -393,8 +407,8 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                     issue_s<HD>(tmem + C::template col_s<FUSED_DQ>(gt), tmem + C::COL_KT,
                                 sdesc_advance(q_km, st0 * C::Q_BYTES), idesc_s);
                     tc_commit(&bars->s_full[TWO_S ? (gt & 1) : 0]);
-                    issue_rows_dot<HD>(tmem + C::COL_DP, v_km, sdesc_advance(do_km, st0 * C::Q_BYTES));
-                    tc_commit(&bars->dp_full);
+                    issue_rows_dot<HD>(tmem + C::template col_dp<FUSED_DQ>(gt), v_km, sdesc_advance(do_km, st0 * C::Q_BYTES));
+                    tc_commit(&bars->dp_full[TWO_DP ? (gt & 1) : 0]);
                 }
                 __syncwarp();
                 for (int it = 0; ok && it < n; ++it) {
@@ -432,6 +446,15 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                                    sdesc_advance(do_mn, qoff + ks * 2048), idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
                     }
                     __syncwarp();
+                    if (TWO_DP && nx < n) {
+                        // next dP^T into the other buffer: its dS^T (tile gi - 1) was read by the dK MMA
+                        // issued one iteration ago; its query stage was waited for with the next S^T
+                        if (leader) {
+                            issue_rows_dot<HD>(tmem + C::template col_dp<FUSED_DQ>(gn), v_km, sdesc_advance(do_km, stn * C::Q_BYTES));
+                            tc_commit(&bars->dp_full[gn & 1]);
+                        }
+                        __syncwarp();
+                    }
                     if (!TWO_S && nx < n) {   // next S^T: its columns are free once the dV MMA above has read P^T
                         if (!(ok = warp_wait(&bars->q_full[stn], (gn / NSQ) & 1, bars, status))) break;
                         tc_fence_after_sync();
@@ -452,12 +475,12 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                     if (leader) {
 #pragma unroll
                         for (int ks = 0; ks < BM / 16; ++ks)
-                            mma_ts(tmem + C::COL_DK, tmem + C::COL_DP + ks * 8, sdesc_advance(q_mn, qoff + ks * 2048),
-                                   idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
+                            mma_ts(tmem + C::COL_DK, tmem + C::template col_dp<FUSED_DQ>(gi) + ks * 8,
+                                   sdesc_advance(q_mn, qoff + ks * 2048), idesc_acc, (it > 0 || ks > 0) ? 1u : 0u);
                         tc_commit(&bars->q_empty[st]);
-                        if (nx < n) {
+                        if (!TWO_DP && nx < n) {
                             issue_rows_dot<HD>(tmem + C::COL_DP, v_km, sdesc_advance(do_km, stn * C::Q_BYTES));
-                            tc_commit(&bars->dp_full);
+                            tc_commit(&bars->dp_full[0]);
                         }
                     }
                     __syncwarp();
@@ -625,7 +648,9 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->p_full);
 
-                if (!(ok = warp_wait(&bars->dp_full, gi & 1, bars, status))) break;
+                if (!(ok = TWO_DP ? warp_wait(&bars->dp_full[b], ph2, bars, status)
+                                  : warp_wait(&bars->dp_full[0], gi & 1, bars, status)))
+                    break;
                 tc_fence_after_sync();
                 // dS buffer b was last read by the dQ^T MMA of tile gi - 2, which the MMA warp issued
                 // before this tile's S^T: the S^T commit waited for above tracks it, so the buffer is
@@ -640,8 +665,9 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                 // all 64 dP columns with one tcgen05.wait::ld (each wait waits for every load in flight;
                 // one wait instead of two per tile measured 1-5 % faster)
                 uint32_t dpa[64];
-                tmem_ld32(tmem + lane_off + C::COL_DP, dpa);
-                tmem_ld32(tmem + lane_off + C::COL_DP + 32, dpa + 32);
+                const uint32_t t_dp = tmem + lane_off + C::template col_dp<FUSED_DQ>(gi);
+                tmem_ld32(t_dp, dpa);
+                tmem_ld32(t_dp + 32, dpa + 32);
                 tmem_wait_ld();
                 reg_fence32(dpa);
                 reg_fence32(dpa + 32);
@@ -663,7 +689,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                         pk[e] = pack_bf16x2(ds.x, ds.y);
                     }
                     // dS^T pairs into the dP^T columns already read (A operand of dK += dS^T Q_i)
-                    tmem_st16(tmem + lane_off + C::COL_DP + 16 * h, pk);
+                    tmem_st16(t_dp + 16 * h, pk);
                     if (FUSED_DQ) {
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
