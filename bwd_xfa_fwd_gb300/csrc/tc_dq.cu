@@ -51,7 +51,7 @@ struct Cfg {
 struct Bars {
     uint64_t qdo_full;
     uint64_t k_full[3], v_full[3], kv_empty[3];
-    uint64_t s_full[2], dp_full, ds_full, done, drain;
+    uint64_t dp_full, ds_full, done, drain;   // dp_full: S and dP of a key tile in TMEM
     uint32_t tmem_base;
     int abort;
 };
@@ -113,8 +113,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->v_full[s], 1);
             mbar_init(&bars->kv_empty[s], 1);
         }
-        mbar_init(&bars->s_full[0], 1);
-        mbar_init(&bars->s_full[1], 1);
         mbar_init(&bars->dp_full, 1);
         mbar_init(&bars->ds_full, 4);   // one arrival per compute warp
         mbar_init(&bars->done, 1);
@@ -182,7 +180,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             if (leader) {
                 issue_rows_dot<HD>(tmem + C::COL_S, q_desc, k_desc);
-                tc_commit(&bars->s_full[0]);
                 issue_rows_dot<HD>(tmem + C::COL_DP, do_desc, v_desc);
                 tc_commit(&bars->dp_full);
             }
@@ -196,7 +193,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after_sync();
                 if (leader) {
                     issue_rows_dot<HD>(tmem + C::COL_S + 128 * (jn & 1), q_desc, sdesc_advance(k_desc, stn * C::TILE_BYTES));
-                    tc_commit(&bars->s_full[jn & 1]);
                 }
                 __syncwarp();
             }
@@ -236,7 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t sc2 = f2_pack(scale, scale);
         bool ok = true;
         for (int j = 0; j < nkv; ++j) {
-            if (!(ok = warp_wait(&bars->s_full[j & 1], (j >> 1) & 1, bars, status))) break;
+            // dP of this tile is issued after its S (the S of tile j goes out before tile j - 1's dS
+            // is waited for, this tile's dP after it), so the dP commit also covers the S: one wait
             if (!(ok = warp_wait(&bars->dp_full, j & 1, bars, status))) break;
             tc_fence_after_sync();
             const uint32_t tS = tmem + lane_off + C::COL_S + 128 * (j & 1);
