@@ -33,7 +33,8 @@
 // Without the fused dQ (the deterministic variant) the dQ^T columns hold a second
 // S^T buffer, and at hd = 64 the columns past K_j do: tiles alternate between the
 // two, and S^T of the next tile is issued before this tile's dV, so the key warps
-// do not wait for it.
+// do not wait for it.  At hd = 64 with the fused dQ a second dP^T buffer follows
+// (columns [416, 480)), so the next tile's dP^T is issued before this tile's dK.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -280,7 +281,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
             mbar_init(&bars->ds_full[b], 4 + (FUSED_DQ && HD == 64 ? HD / 32 : 0));
             mbar_init(&bars->ds_empty[b], 1);
             mbar_init(&bars->item_full[b], 1);
-            // MMA warp, four key warps, four readout warps (+ four mask warps)
+            // MMA warp, four key warps, four readout warps (+ the keep-bit warps)
             mbar_init(&bars->item_empty[b], 9 + (DROP ? kMaskWarps : 0));
         }
         mbar_init(&bars->s_full[0], 1);
@@ -317,7 +318,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     const uint32_t *mask_s = reinterpret_cast<const uint32_t *>(smem + C::OFF_MASK);
 
     // Roles by warpgroup (with dropout every warpgroup first resizes its registers, all four warps
-    // together): warps 8-11 the TMA and MMA warps (and two idle ones), 12-15 the keep-bit warps,
+    // together): warps 8-11 the TMA and MMA warps (and two idle ones), 12-19 the keep-bit warps,
     // 0-3 the key-row warps, 4-7 the dQ readout warps.
     if (warp >= 8 && warp < 12) {
         if (DROP) regs_decrease<56>();

@@ -86,7 +86,7 @@ struct Bars {
     uint64_t mask_full[2][MS];   // keep bits of tile t written (one arrival per mask warp)
     uint64_t mask_empty[2][MS];  // read by the softmax group of tile t (one arrival per warp)
     uint64_t item_full[2];   // work-item id posted by the TMA warp
-    uint64_t item_empty[2];  // id read by the MMA warp and the eight softmax warps
+    uint64_t item_empty[2];  // id read by the MMA warp, the eight softmax warps and any keep-bit warps
     int item_id[2];          // the posted ids (-1: no more work)
     uint32_t tmem_base;
     int abort;
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
         mbar_init(&bars->drain, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->item_full[i], 1);
-            // MMA warp + eight softmax warps (+ four mask warps)
+            // MMA warp + eight softmax warps (+ the keep-bit warps)
             mbar_init(&bars->item_empty[i], 1 + BM / 32 * 2 + (DROP ? kMaskWarps : 0));
         }
         for (int t = 0; t < 2; ++t)
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     uint32_t *mask_s = reinterpret_cast<uint32_t *>(smem + C::OFF_MASK);
 
     // Roles by warpgroup (with dropout every warpgroup first resizes its registers, all four warps
-    // together): warps 8-11 the TMA and MMA warps (and two idle ones), 12-15 the keep-bit warps,
+    // together): warps 8-11 the TMA and MMA warps (and two idle ones), 12-19 the keep-bit warps,
     // 0-7 the softmax groups.
     if (warp >= 8 && warp < 12) {
         if (DROP) regs_decrease<56>();
