@@ -379,6 +379,8 @@ def run_ours(args, w):
     out, lse = torch.empty_like(q), torch.empty(q.shape[:-1], device="cuda", dtype=torch.float32)
     grads = tuple(torch.empty_like(q) for _ in range(3))
     ws = torch.empty(binding.workspace_bytes(w.bh, w.S, w.hd, q.dtype), device="cuda", dtype=torch.uint8)
+    keep = (torch.empty(binding.dropout_keep_bytes(w.bh, w.S), device="cuda", dtype=torch.uint8)
+            if args.dropout and args.keep_bits else None)
     stream = torch.cuda.current_stream()
 
     impl = FAMILIES[args.family]
@@ -407,14 +409,16 @@ def run_ours(args, w):
         mark("fwd", 0)
         if args.dropout:
             # dropout on the attention probabilities: the backward is one xfa_bwd_dropout call
-            # (its pre-pass, kernel and conversion), timed as "main"
-            binding.fwd(q, k, v, w.scale, impl, out=out, lse=lse, dropout_p=args.dropout, seed=DROPOUT_SEED)
+            # (its pre-pass, kernel and conversion), timed as "main"; with --keep-bits the pair
+            # caches the forward's keep decisions (xfa_fwd_dropout_keep / xfa_bwd_dropout_keep)
+            binding.fwd(q, k, v, w.scale, impl, out=out, lse=lse, dropout_p=args.dropout, seed=DROPOUT_SEED,
+                        keep_bits=keep)
             mark("fwd", 1)
             mark("prep", 0)
             mark("prep", 1)
             mark("main", 0)
             binding.bwd(q, k, v, out, do, lse, w.scale, impl, workspace=ws, grads=grads, dropout_p=args.dropout,
-                        seed=DROPOUT_SEED)
+                        seed=DROPOUT_SEED, keep_bits=keep)
             mark("main", 1)
             mark("finish", 0)
             mark("finish", 1)
@@ -487,7 +491,8 @@ def run_ours(args, w):
         "dtype": w.dtype,
         "data": data_note(w),
         "config": dict(workload_config(w),
-                       **({"dropout_p": args.dropout, "dropout_seed": DROPOUT_SEED} if args.dropout else {})),
+                       **({"dropout_p": args.dropout, "dropout_seed": DROPOUT_SEED} if args.dropout else {}),
+                       **({"dropout_keep_bits": True} if args.dropout and args.keep_bits else {})),
         "kernel_family": args.family,
         "fwd_tflops": f_fwd / (per["fwd"] * 1e-3) / 1e12,
         "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
@@ -542,6 +547,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="dropout rate on the attention probabilities (0: none, the benchmark's default)")
+    ap.add_argument("--keep-bits", action="store_true",
+                    help="with --dropout: cache the forward's keep decisions for the backward "
+                         "(xfa_fwd_dropout_keep / xfa_bwd_dropout_keep) instead of drawing them twice")
     ap.add_argument("--family", choices=sorted(FAMILIES), default="auto",
                     help="kernel family (xfa_impl): auto, tcgen05 (bf16: dQ by fp32 reductions; fp32 with "
                          "hd 32/64: the 3xTF32 kernels), tcgen05_det (bf16: dQ by a separate pass, "

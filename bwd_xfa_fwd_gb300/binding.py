@@ -46,6 +46,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "xfa_bwd": ([vp] * 9 + [i, i, i, f, i, vp, sz, vp], i),
         "xfa_bwd_impl": ([vp] * 9 + [i, i, i, f, i, vp, sz, i, vp], i),
         "xfa_bwd_dropout": ([vp] * 9 + [i, i, i, f, i, f, u64, vp, sz, i, vp], i),
+        "xfa_dropout_keep_bytes": ([i, i], sz),
+        "xfa_fwd_dropout_keep": ([vp, vp, vp, vp, vp, i, i, i, f, i, f, u64, vp, sz, i, vp], i),
+        "xfa_bwd_dropout_keep": ([vp] * 9 + [i, i, i, f, i, f, vp, sz, vp, sz, i, vp], i),
         "xfa_bwd_prep": ([vp, vp, vp, vp, i, i, i, i, vp, sz, i, vp], i),
         "xfa_bwd_main": ([vp] * 7 + [i, i, i, f, i, vp, sz, i, vp], i),
         "xfa_bwd_finish": ([vp, i, i, i, i, vp, sz, i, vp], i),
@@ -82,6 +85,12 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _nbytes(t: torch.Tensor) -> int:
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("keep_bits must be a contiguous CUDA tensor")
+    return t.numel() * t.element_size()
+
+
 def _shape3(q: torch.Tensor):
     """[bh, S, hd] or [B, H, S, hd] (contiguous) -> (bh, S, hd)."""
     if q.dim() == 3:
@@ -104,17 +113,28 @@ def default_scale(hd: int) -> float:
     return 1.0 / math.sqrt(hd)
 
 
+def dropout_keep_bytes(bh: int, S: int) -> int:
+    """Bytes of the keep-bit cache of a dropout forward / backward pair (xfa_dropout_keep_bytes)."""
+    return int(load().xfa_dropout_keep_bytes(bh, S))
+
+
 def fwd(q, k, v, scale: float | None = None, impl: int = IMPL_AUTO, out=None, lse=None, dropout_p: float = 0.0,
-        seed: int = 0):
+        seed: int = 0, keep_bits=None):
     """Forward: returns (O, L).  O has q's shape/dtype; L is fp32 [..., S].  ``dropout_p`` > 0
     applies dropout of that rate to the attention probabilities (xfa_fwd_dropout); the
-    backward must get the same ``dropout_p`` and ``seed``."""
+    backward must get the same ``dropout_p`` and ``seed``.  With ``keep_bits`` (a CUDA uint8
+    tensor of at least :func:`dropout_keep_bytes` bytes) the forward also caches its keep
+    decisions there (xfa_fwd_dropout_keep) for a backward given the same tensor."""
     _check_tensors(q, k, v)
     bh, S, hd = _shape3(q)
     scale = default_scale(hd) if scale is None else float(scale)
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty(q.shape[:-1], device=q.device, dtype=torch.float32) if lse is None else lse
-    if dropout_p:
+    if dropout_p and keep_bits is not None:
+        _check(load().xfa_fwd_dropout_keep(_p(q), _p(k), _p(v), _p(out), _p(lse), bh, S, hd, scale, _DTYPE[q.dtype],
+                                           float(dropout_p), int(seed) % 2 ** 64, _p(keep_bits), _nbytes(keep_bits),
+                                           impl, _stream(q)), "xfa_fwd_dropout_keep")
+    elif dropout_p:
         _check(load().xfa_fwd_dropout(_p(q), _p(k), _p(v), _p(out), _p(lse), bh, S, hd, scale, _DTYPE[q.dtype],
                                       float(dropout_p), int(seed) % 2 ** 64, impl, _stream(q)), "xfa_fwd_dropout")
     else:
@@ -128,9 +148,11 @@ def workspace_bytes(bh: int, S: int, hd: int, dtype: torch.dtype) -> int:
 
 
 def bwd(q, k, v, out, dout, lse, scale: float | None = None, impl: int = IMPL_AUTO, workspace=None, grads=None,
-        dropout_p: float = 0.0, seed: int = 0):
+        dropout_p: float = 0.0, seed: int = 0, keep_bits=None):
     """Backward: returns (dQ, dK, dV), each of q's shape/dtype (overwritten).  ``dropout_p`` and
-    ``seed`` must be those of the forward (xfa_bwd_dropout when ``dropout_p`` > 0)."""
+    ``seed`` must be those of the forward (xfa_bwd_dropout when ``dropout_p`` > 0); with
+    ``keep_bits``, the forward's cached decisions are read instead of drawn (xfa_bwd_dropout_keep,
+    no seed needed)."""
     _check_tensors(q, k, v, out, dout)
     bh, S, hd = _shape3(q)
     scale = default_scale(hd) if scale is None else float(scale)
@@ -138,7 +160,12 @@ def bwd(q, k, v, out, dout, lse, scale: float | None = None, impl: int = IMPL_AU
     if workspace is None:
         workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
     dq, dk, dv = grads if grads is not None else (torch.empty_like(q), torch.empty_like(q), torch.empty_like(q))
-    if dropout_p:
+    if dropout_p and keep_bits is not None:
+        _check(load().xfa_bwd_dropout_keep(_p(q), _p(k), _p(v), _p(out), _p(dout), _p(lse), _p(dq), _p(dk), _p(dv),
+                                           bh, S, hd, scale, _DTYPE[q.dtype], float(dropout_p), _p(keep_bits),
+                                           _nbytes(keep_bits), _p(workspace), workspace.numel(), impl, _stream(q)),
+               "xfa_bwd_dropout_keep")
+    elif dropout_p:
         _check(load().xfa_bwd_dropout(_p(q), _p(k), _p(v), _p(out), _p(dout), _p(lse), _p(dq), _p(dk), _p(dv), bh, S,
                                       hd, scale, _DTYPE[q.dtype], float(dropout_p), int(seed) % 2 ** 64,
                                       _p(workspace), workspace.numel(), impl, _stream(q)), "xfa_bwd_dropout")

@@ -48,7 +48,7 @@ template <typename VecT, int HD, int ELT, bool PREP>
 __global__ void __launch_bounds__(256) rowdot_kernel(const VecT *__restrict__ O, const VecT *__restrict__ dO,
                                                      const float *__restrict__ lse, float *__restrict__ D,
                                                      float *__restrict__ Lg, float *__restrict__ zero_acc, int S,
-                                                     int S_pad, long total_rows)
+                                                     int S_pad, long total_rows, float lg_bias)
 {
     constexpr int VEC = 16 / ELT;      // elements per 16-byte vector
     constexpr int LPR = HD / VEC;      // lanes per row
@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(256) rowdot_kernel(const VecT *__restrict__ O,
         for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (valid && sub == 0) {
             D[r] = acc;
-            if (PREP) Lg[r] = real ? -lse[b * S + i] * kLog2e : -CUDART_INF_F;
+            if (PREP) Lg[r] = real ? -lse[b * S + i] * kLog2e + lg_bias : -CUDART_INF_F;
         }
         if (PREP && real && zero_acc) {
             // clear this row of the fp32 dQ accumulator: HD floats over the LPR lanes of the row
@@ -93,7 +93,7 @@ int sm_count()
 
 template <int HD>
 cudaError_t rowdot_launch(const void *O, const void *dO, const float *lse, float *D, float *Lg, float *zero_acc,
-                          int bh, int S, int S_pad, int dtype, bool prep, cudaStream_t st)
+                          int bh, int S, int S_pad, int dtype, bool prep, float lg_bias, cudaStream_t st)
 {
     const long rows = (long)bh * S_pad;
     const int sms = sm_count();
@@ -102,28 +102,28 @@ cudaError_t rowdot_launch(const void *O, const void *dO, const float *lse, float
     if (dtype == XFA_BF16) {
         if (prep)
             rowdot_kernel<uint4, HD, 2, true><<<grid, 256, 0, st>>>((const uint4 *)O, (const uint4 *)dO, lse, D, Lg,
-                                                                     zero_acc, S, S_pad, rows);
+                                                                     zero_acc, S, S_pad, rows, lg_bias);
         else
             rowdot_kernel<uint4, HD, 2, false><<<grid, 256, 0, st>>>((const uint4 *)O, (const uint4 *)dO, lse, D,
-                                                                      Lg, zero_acc, S, S_pad, rows);
+                                                                      Lg, zero_acc, S, S_pad, rows, lg_bias);
     } else {
         if (prep)
             rowdot_kernel<float4, HD, 4, true><<<grid, 256, 0, st>>>((const float4 *)O, (const float4 *)dO, lse, D,
-                                                                      Lg, zero_acc, S, S_pad, rows);
+                                                                      Lg, zero_acc, S, S_pad, rows, lg_bias);
         else
             rowdot_kernel<float4, HD, 4, false><<<grid, 256, 0, st>>>((const float4 *)O, (const float4 *)dO, lse,
-                                                                       D, Lg, zero_acc, S, S_pad, rows);
+                                                                       D, Lg, zero_acc, S, S_pad, rows, lg_bias);
     }
     return cudaGetLastError();
 }
 
 cudaError_t rowdot_any(const void *O, const void *dO, const float *lse, float *D, float *Lg, float *zero_acc, int bh,
-                       int S, int S_pad, int hd, int dtype, bool prep, cudaStream_t st)
+                       int S, int S_pad, int hd, int dtype, bool prep, float lg_bias, cudaStream_t st)
 {
     switch (hd) {
-    case 32: return rowdot_launch<32>(O, dO, lse, D, Lg, zero_acc, bh, S, S_pad, dtype, prep, st);
-    case 64: return rowdot_launch<64>(O, dO, lse, D, Lg, zero_acc, bh, S, S_pad, dtype, prep, st);
-    case 128: return rowdot_launch<128>(O, dO, lse, D, Lg, zero_acc, bh, S, S_pad, dtype, prep, st);
+    case 32: return rowdot_launch<32>(O, dO, lse, D, Lg, zero_acc, bh, S, S_pad, dtype, prep, lg_bias, st);
+    case 64: return rowdot_launch<64>(O, dO, lse, D, Lg, zero_acc, bh, S, S_pad, dtype, prep, lg_bias, st);
+    case 128: return rowdot_launch<128>(O, dO, lse, D, Lg, zero_acc, bh, S, S_pad, dtype, prep, lg_bias, st);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -194,13 +194,13 @@ unsigned elementwise_grid(size_t n)
 
 cudaError_t launch_bwd_prep(const BwdParams &p, cudaStream_t st)
 {
-    return rowdot_any(p.out, p.dout, p.lse, p.D, p.Lg, p.dq_acc, p.bh, p.S, p.S_pad, p.hd, p.dtype, true, st);
+    return rowdot_any(p.out, p.dout, p.lse, p.D, p.Lg, p.dq_acc, p.bh, p.S, p.S_pad, p.hd, p.dtype, true, p.lg_bias, st);
 }
 
 cudaError_t launch_rowdot(const void *out, const void *dout, float *d, int bh, int S, int hd, int dtype,
                           cudaStream_t st)
 {
-    return rowdot_any(out, dout, nullptr, d, nullptr, nullptr, bh, S, S, hd, dtype, false, st);
+    return rowdot_any(out, dout, nullptr, d, nullptr, nullptr, bh, S, S, hd, dtype, false, 0.0f, st);
 }
 
 cudaError_t launch_convert_dq(const float *acc, void *dq, size_t n, int dtype, cudaStream_t st)

@@ -16,12 +16,29 @@ namespace xfa {
 // [bh, S, S] probabilities is kept when the 24-bit draw of its flat index is >= keep_thr
 // (= ceil(p * 2^24), so the test equals u = draw / 2^24 >= p exactly) and then scaled by
 // inv_keep = 1 / (1 - p).  on == false: no dropout (the plain kernels run).
+// keep_out / keep_in: the decisions cached as bits between the forward and the backward (the
+// tensor-core bf16 kernels only; see keep_word in dropout.cuh for the layout): the forward also
+// writes every decision it draws to keep_out, the backward reads them from keep_in instead of
+// drawing them again.  keep_nkt / keep_w: key tiles and query-row words of that layout.
 struct DropParams {
     bool on = false;
     uint32_t keep_thr = 0;
     float inv_keep = 1.0f;
+    float keep_frac = 1.0f;   // 1 - p
     uint64_t seed = 0;
+    uint32_t *keep_out = nullptr;
+    const uint32_t *keep_in = nullptr;
+    int keep_nkt = 0, keep_w = 0;
 };
+
+// Key tiles (128 keys) and query-row words (32 rows, for the query blocks of 256 rows the
+// forward works in) of the cached keep bits of a [bh, S, S] probability tensor.
+inline int keep_key_tiles(int S) { return (S + 127) / 128; }
+inline int keep_row_words(int S) { return 8 * ((S + 255) / 256); }
+inline size_t keep_bits_bytes(int bh, int S)
+{
+    return (size_t)bh * (size_t)keep_key_tiles(S) * (size_t)keep_row_words(S) * 128u * 4u;
+}
 
 struct FwdParams {
     const void *q, *k, *v;
@@ -46,6 +63,7 @@ struct BwdParams {
     float *Lg;      // [bh][S_pad]  -L_i * log2(e) (-inf on padded rows)
     float *dq_acc;  // [bh][S][hd]  fp32 dQ accumulator (== dq when dtype is fp32)
     int S_pad;
+    float lg_bias = 0.0f;   // added to Lg by the pre-pass (log2(1 / (1 - p)) for the tcgen05 dropout backward)
     int *status;
     DropParams drop;
 };

@@ -298,7 +298,8 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
         if (DROP) {
             MaskBars *mb = reinterpret_cast<MaskBars *>(smem + C::OFF_MBAR);
             for (int s = 0; s < MSB; ++s) {
-                mbar_init(&mb->full[s], kMaskWarps);
+                // drawn: one arrival per keep-bit warp; cached: one bulk copy (arrival + bytes)
+                mbar_init(&mb->full[s], drop.keep_in ? 1 : kMaskWarps);
                 mbar_init(&mb->empty[s], 4);
             }
         }
@@ -514,36 +515,69 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     } else if (warp >= 12) {
         if (DROP) {
             regs_decrease<56>();
-            // keep bits (dropout): thread = key r of the item's key tile, half m of the query rows;
-            // for every query tile, in the order the key-row warps consume them, the 32 decisions of
-            // (row i0 + 32m + c, key) as one 32-bit word, element drawn from its flat index
-            // (head*S + i0 + 32m + c)*S + key
-            const int mw = warp - kWarpMask0;
-            const int r = (mw % 4) * 32 + lane, m = mw / 4;
+            // keep bits (dropout) of every query tile, in the order the key-row warps consume them, as
+            // two 128-word rows per stage (row m: bit c of word r = decision of (row i0 + 32m + c, key r)).
             uint32_t *mask_w = reinterpret_cast<uint32_t *>(smem + C::OFF_MASK);
+            const int mw = warp - kWarpMask0;
             uint32_t nm = 0;   // stages filled
             bool ok = true;
-            for (int k = 0; ok; ++k) {
-                const int item = take_item(bars, k, status, ok);
-                if (item < 0) break;
-                const Item w = item_of(item);
-                const uint64_t key = (uint64_t)(w.j0 + r);
-                const uint64_t step = (uint64_t)S * kDropGolden;
-                for (int it = 0; it < w.n; ++it) {
-                    const uint32_t st = nm % MSB;
-                    if (nm >= MSB && !(ok = warp_wait(&mbars->empty[st], ((nm / MSB) + 1) & 1, bars, status))) break;
-                    const uint64_t i0 = (uint64_t)((w.it0 + it) * BM + 32 * m);
-                    uint64_t g = (((uint64_t)w.head * S + i0) * (uint64_t)S + key) * kDropGolden;
-                    uint32_t bits = 0u;
-#pragma unroll 4
-                    for (int b = 0; b < 32; ++b) {
-                        bits |= (uint32_t)drop_keep(drop.seed, g, drop.keep_thr) << b;
-                        g += step;
+            if (drop.keep_in) {
+                // cached by the forward in the same order (keep_word): one thread copies each tile's
+                // 1 KB with a bulk copy, up to MSB tiles ahead; the other keep-bit warps only take items
+                const bool lead = mw == 0;
+                const bool issuer = lead && elect_one();
+                const int issuer_lane = lead ? __ffs(__ballot_sync(0xffffffffu, issuer)) - 1 : 0;
+                uint32_t last[MSB] = {};   // 1 + last tile copied per stage
+                for (int k = 0; ok; ++k) {
+                    const int item = take_item(bars, k, status, ok);
+                    if (item < 0) break;
+                    const Item w = item_of(item);
+                    if (issuer) {
+                        for (int it = 0; it < w.n; ++it, ++nm) {
+                            const uint32_t st = nm % MSB;
+                            if (nm >= MSB && !(ok = mbar_wait(&mbars->empty[st], ((nm / MSB) + 1) & 1, &bars->abort))) break;
+                            mbar_arrive_expect_tx(&mbars->full[st], 2 * BN * 4);
+                            bulk_load(mask_w + st * 2 * BN,
+                                      drop.keep_in + keep_word(w.head, w.j0 / BN, 2 * (w.it0 + it), 0, drop.keep_nkt, drop.keep_w),
+                                      2 * BN * 4, &mbars->full[st]);
+                            last[st] = nm + 1;
+                        }
                     }
-                    mask_w[(st * BN + r) * 2 + m] = bits;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&mbars->full[st]);
-                    ++nm;
+                    if (lead) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, issuer_lane) != 0;   // warp-uniform again
+                }
+                if (issuer) {
+                    if (!ok) fail(bars, status);
+                    // never leave the CTA with copies in flight
+                    for (int st = 0; st < MSB; ++st)
+                        if (last[st]) mbar_wait(&mbars->full[st], ((last[st] - 1) / MSB) & 1, nullptr);
+                }
+            } else {
+                // drawn: thread = key r of the item's key tile, half m of the query rows; the 32
+                // decisions of (row i0 + 32m + c, key) as one word, element drawn from its flat index
+                // (head*S + i0 + 32m + c)*S + key
+                const int r = (mw % 4) * 32 + lane, m = mw / 4;
+                for (int k = 0; ok; ++k) {
+                    const int item = take_item(bars, k, status, ok);
+                    if (item < 0) break;
+                    const Item w = item_of(item);
+                    const uint64_t key = (uint64_t)(w.j0 + r);
+                    const uint64_t step = (uint64_t)S * kDropGolden;
+                    for (int it = 0; it < w.n; ++it) {
+                        const uint32_t st = nm % MSB;
+                        if (nm >= MSB && !(ok = warp_wait(&mbars->empty[st], ((nm / MSB) + 1) & 1, bars, status))) break;
+                        const uint64_t i0 = (uint64_t)((w.it0 + it) * BM + 32 * m);
+                        uint64_t g = (((uint64_t)w.head * S + i0) * (uint64_t)S + key) * kDropGolden;
+                        uint32_t bits = 0u;
+#pragma unroll 4
+                        for (int b = 0; b < 32; ++b) {
+                            bits |= (uint32_t)drop_keep(drop.seed, g, drop.keep_thr) << b;
+                            g += step;
+                        }
+                        mask_w[(st * 2 + m) * BN + r] = bits;
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&mbars->full[st]);
+                        ++nm;
+                    }
                 }
             }
         }
@@ -595,9 +629,8 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                 if (DROP) {
                     const uint32_t mst = gi % MSB;
                     if (!(ok = warp_wait(&mbars->full[mst], (gi / MSB) & 1, bars, status))) break;
-                    const uint2 v = *reinterpret_cast<const uint2 *>(mask_s + (mst * BN + r) * 2);
-                    km[0] = v.x;
-                    km[1] = v.y;
+                    km[0] = mask_s[(mst * 2) * BN + r];
+                    km[1] = mask_s[(mst * 2 + 1) * BN + r];
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&mbars->empty[mst]);
                 }
@@ -613,7 +646,9 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                 tmem_wait_ld();
                 reg_fence32(sr);
                 reg_fence32(sr + 32);
-                // p = 2^(s * scale * log2(e) - L * log2(e)) on packed pairs; -L*log2(e) comes from the pre-pass
+                // p = 2^(s * scale * log2(e) - L * log2(e)) on packed pairs; -L*log2(e) comes from the pre-pass.
+                // With dropout the pre-pass adds log2(1 / (1 - p_drop)), so p here is already P / (1 - p_drop):
+                // P o C is p where the key is kept and 0 elsewhere, and dS (below) takes D (1 - p_drop) in place of D
                 const uint64_t cs2 = f2_pack(scale_log2, scale_log2);
                 const bool diag = key > i0;   // some (key > row) pairs in this tile
                 uint64_t pp[32];              // P pairs (fp32) kept for dS
@@ -636,7 +671,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                             if (DROP) {
                                 const bool k0 = (km[cc / 32] >> (cc % 32)) & 1u;
                                 const bool k1 = (km[cc / 32] >> (cc % 32 + 1)) & 1u;
-                                pk[cc / 2] = pack_bf16x2(k0 ? p0 * drop.inv_keep : 0.0f, k1 ? p1 * drop.inv_keep : 0.0f);
+                                pk[cc / 2] = pack_bf16x2(k0 ? p0 : 0.0f, k1 ? p1 : 0.0f);
                             } else {
                                 pk[cc / 2] = pack_bf16x2(p0, p1);
                             }
@@ -660,9 +695,10 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                 if (FUSED_DQ && HD == 128 && gi >= 2 && !(ok = warp_wait(&bars->ds_empty[b], ph2 ^ 1, bars, status)))
                     break;
                 uint8_t *dsrow = smem + C::OFF_DS + b * C::DS_BYTES + r * 128;
-                // dS = P (dP - D) scale on packed pairs
+                // dS = P (dP - D) scale on packed pairs; with dropout P (C dP / (1 - p_drop) - D) scale, formed
+                // as p (C dP - (1 - p_drop) D) scale from the p / (1 - p_drop) above
                 const uint64_t sc2 = f2_pack(scale, scale);
-                const uint64_t m1 = f2_pack(-1.0f, -1.0f);
+                const uint64_t m1 = DROP ? f2_pack(-drop.keep_frac, -drop.keep_frac) : f2_pack(-1.0f, -1.0f);
                 // all 64 dP columns with one tcgen05.wait::ld (each wait waits for every load in flight;
                 // one wait instead of two per tile measured 1-5 % faster)
                 uint32_t dpa[64];
@@ -681,9 +717,9 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                         const int c = 32 * h + 2 * e;
                         const float2 d2 = *reinterpret_cast<const float2 *>(Ds + c);
                         float dp0 = __uint_as_float(dp[2 * e]), dp1 = __uint_as_float(dp[2 * e + 1]);
-                        if (DROP) {   // the dropout node's backward: dP = C o (dO V^T)
-                            dp0 = (km[c / 32] >> (c % 32)) & 1u ? dp0 * drop.inv_keep : 0.0f;
-                            dp1 = (km[c / 32] >> (c % 32 + 1)) & 1u ? dp1 * drop.inv_keep : 0.0f;
+                        if (DROP) {   // the dropout node's backward: C o (dO V^T), its 1 / (1 - p_drop) in p
+                            dp0 = (km[c / 32] >> (c % 32)) & 1u ? dp0 : 0.0f;
+                            dp1 = (km[c / 32] >> (c % 32 + 1)) & 1u ? dp1 : 0.0f;
                         }
                         const uint64_t t = ffma2(f2_pack(d2.x, d2.y), m1, f2_pack(dp0, dp1));
                         const float2 ds = f2_unpack(fmul2(fmul2(pp[c / 2], sc2), t));

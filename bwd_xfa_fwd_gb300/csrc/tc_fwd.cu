@@ -430,6 +430,14 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&bars->mask_full[t][st]);
                         ++nm[t];
+                        if (drop.keep_out) {
+                            // the same decisions kept for the backward: one word per key over this
+                            // warp's 32 rows (keep_word), 128 contiguous bytes per store
+                            const int wrow = (q0 + t * BM + (mw % 4) * 32) / 32;
+                            uint32_t *dst = drop.keep_out + keep_word(head, j, wrow, 64 * m + lane, drop.keep_nkt, drop.keep_w);
+                            dst[0] = warp_transpose_bits32(w[0], lane);
+                            dst[32] = warp_transpose_bits32(w[1], lane);
+                        }
                     }
                 }
             }
@@ -544,9 +552,9 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                         const float p1 = ex2_approx(a.y);
                         l2[e & 3] = fadd2(l2[e & 3], f2_pack(p0, p1));
                         if (DROP) {
-                            // keys j*BN + c, c + 1 of this row
-                            const float d0 = (kb[c >> 5] >> (c & 31)) & 1u ? p0 * drop.inv_keep : 0.0f;
-                            const float d1 = (kb[c >> 5] >> ((c + 1) & 31)) & 1u ? p1 * drop.inv_keep : 0.0f;
+                            // keys j*BN + c, c + 1 of this row; the factor 1 / (1 - p_drop) is applied to O once, at the end
+                            const float d0 = (kb[c >> 5] >> (c & 31)) & 1u ? p0 : 0.0f;
+                            const float d1 = (kb[c >> 5] >> ((c + 1) & 31)) & 1u ? p1 : 0.0f;
                             pk[e] = pack_bf16x2(d0, d1);
                         } else {
                             pk[e] = pack_bf16x2(p0, p1);
@@ -568,7 +576,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
             ++no;
             {
                 tc_fence_after_sync();
-                const float inv_l = 1.0f / l;
+                const float inv_l = (DROP ? drop.inv_keep : 1.0f) / l;
                 __nv_bfloat16 *orow = O + ((size_t)head * S + row) * HD;
 #pragma unroll 1
                 for (int c = 0; c < HD; c += 32) {

@@ -229,7 +229,19 @@ static int make_drop(float p, unsigned long long seed, DropParams *d)
     d->on = true;
     d->keep_thr = (uint32_t)ceil((double)p * 16777216.0);   // u = draw / 2^24 >= p  <=>  draw >= keep_thr
     d->inv_keep = (float)(1.0 / (1.0 - (double)p));
+    d->keep_frac = (float)(1.0 - (double)p);
     d->seed = seed;
+    return XFA_OK;
+}
+
+// The cached keep-bit buffer of a dropout call (see DropParams): present, 16-byte aligned and at
+// least xfa_dropout_keep_bytes(bh, S) long; sets the layout sizes.
+static int keep_args(int bh, int S, const void *keep, size_t keep_bytes, DropParams *d)
+{
+    if (bh < 1 || S < 1 || (long long)bh * (long long)S >= (1ll << 26)) return XFA_ERR_INVALID_ARG;
+    if (!keep || !aligned16(keep) || keep_bytes < keep_bits_bytes(bh, S)) return XFA_ERR_INVALID_ARG;
+    d->keep_nkt = keep_key_tiles(S);
+    d->keep_w = keep_row_words(S);
     return XFA_OK;
 }
 
@@ -242,6 +254,8 @@ static int fwd_run(const void *q, const void *k, const void *v, void *out, float
         return XFA_ERR_INVALID_ARG;
     Family fam;
     if ((rc = choose_impl(impl, hd, dtype, &fam)) != XFA_OK) return rc;
+    // cached keep bits: the tensor-core bf16 kernels only
+    if (drop.keep_out && fam != Family::TcFused && fam != Family::TcDet) return XFA_ERR_UNSUPPORTED;
     FwdParams p{q, k, v, out, lse, bh, S, hd, scale, dtype, nullptr};
     p.drop = drop;
     if ((rc = status_ptr(&p.status)) != XFA_OK) return rc;
@@ -265,6 +279,23 @@ int xfa_fwd_dropout(const void *q, const void *k, const void *v, void *out, floa
     DropParams d;
     const int rc = make_drop(p_drop, seed, &d);
     if (rc != XFA_OK) return rc;
+    return fwd_run(q, k, v, out, lse, bh, S, hd, scale, dtype, d, impl, stream);
+}
+
+size_t xfa_dropout_keep_bytes(int bh, int S)
+{
+    if (bh < 1 || S < 1 || (long long)bh * (long long)S >= (1ll << 26)) return 0;
+    return keep_bits_bytes(bh, S);
+}
+
+int xfa_fwd_dropout_keep(const void *q, const void *k, const void *v, void *out, float *lse, int bh, int S, int hd,
+                         float scale, int dtype, float p_drop, unsigned long long seed, void *keep_bits,
+                         size_t keep_bytes, int impl, void *stream)
+{
+    DropParams d;
+    int rc = make_drop(p_drop, seed, &d);
+    if (rc != XFA_OK || (rc = keep_args(bh, S, keep_bits, keep_bytes, &d)) != XFA_OK) return rc;
+    if (d.on) d.keep_out = static_cast<uint32_t *>(keep_bits);
     return fwd_run(q, k, v, out, lse, bh, S, hd, scale, dtype, d, impl, stream);
 }
 
@@ -385,6 +416,9 @@ static int bwd_run(const void *q, const void *k, const void *v, const void *out,
     Family fam;
     if ((rc = choose_impl(impl, hd, dtype, &fam)) != XFA_OK) return rc;
     if (drop.on && fam == Family::TcDet) return XFA_ERR_UNSUPPORTED;   // dropout: every family but bf16 TcDet
+    if (drop.keep_in && fam != Family::TcFused) return XFA_ERR_UNSUPPORTED;   // cached keep bits: bf16 tcgen05
+    // the tcgen05 dropout backward takes P / (1 - p) straight from the exponential: 2^(s c - L log2 e + log2(1 / (1 - p)))
+    if (drop.on && fam == Family::TcFused) p.lg_bias = (float)std::log2((double)drop.inv_keep);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if ((rc = stage_prep(p, fam, st)) != XFA_OK) return rc;
     if ((rc = stage_main(p, fam, st)) != XFA_OK) return rc;
@@ -409,6 +443,19 @@ int xfa_bwd_dropout(const void *q, const void *k, const void *v, const void *out
     DropParams d;
     const int rc = make_drop(p_drop, seed, &d);
     if (rc != XFA_OK) return rc;
+    return bwd_run(q, k, v, out, dout, lse, dq, dk, dv, bh, S, hd, scale, dtype, workspace, workspace_bytes, d, impl,
+                   stream);
+}
+
+int xfa_bwd_dropout_keep(const void *q, const void *k, const void *v, const void *out, const void *dout,
+                         const float *lse, void *dq, void *dk, void *dv, int bh, int S, int hd, float scale,
+                         int dtype, float p_drop, const void *keep_bits, size_t keep_bytes, void *workspace,
+                         size_t workspace_bytes, int impl, void *stream)
+{
+    DropParams d;
+    int rc = make_drop(p_drop, 0, &d);
+    if (rc != XFA_OK || (rc = keep_args(bh, S, keep_bits, keep_bytes, &d)) != XFA_OK) return rc;
+    if (d.on) d.keep_in = static_cast<const uint32_t *>(keep_bits);
     return bwd_run(q, k, v, out, dout, lse, dq, dk, dv, bh, S, hd, scale, dtype, workspace, workspace_bytes, d, impl,
                    stream);
 }

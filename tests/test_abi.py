@@ -73,3 +73,35 @@ def test_host_validation(lib):
     assert lib.xfa_accumulate(None, None, 4, 0, None) == b.XFA_ERR_INVALID_ARG
     assert lib.xfa_accumulate(None, None, 0, 0, None) == b.XFA_OK
     assert lib.xfa_selftest_timeout(0, None) == b.XFA_ERR_INVALID_ARG
+
+
+def test_dropout_keep_bytes_and_validation(lib):
+    """The keep-bit cache of the dropout pair: its size (key tiles of 128 x query-row words of
+    32, 128 words each) and the host checks of the buffer and of the family."""
+    from bwd_xfa_fwd_gb300 import binding as b
+    kb = lib.xfa_dropout_keep_bytes
+    assert kb(2, 300) == 2 * 3 * 16 * 128 * 4      # ceil(300/128) key tiles, 8 * ceil(300/256) words
+    assert kb(32, 8192) == 32 * 64 * 256 * 128 * 4
+    assert kb(0, 64) == 0 and kb(1, 0) == 0 and kb(1 << 13, 1 << 13) == 0
+    good = [ctypes.c_void_p(4096 * (i + 1)) for i in range(5)]
+    need = kb(1, 8)
+    keep = ctypes.c_void_p(1 << 20)
+
+    def fwd_keep(buf, nbytes, impl=b.IMPL_SIMT, p=0.1):
+        return lib.xfa_fwd_dropout_keep(*good, 1, 8, 64, ctypes.c_float(0.125), b.XFA_BF16, ctypes.c_float(p), 7,
+                                        buf, nbytes, impl, None)
+
+    assert fwd_keep(None, need) == b.XFA_ERR_INVALID_ARG
+    assert fwd_keep(ctypes.c_void_p((1 << 20) + 4), need) == b.XFA_ERR_INVALID_ARG
+    assert fwd_keep(keep, need - 1) == b.XFA_ERR_INVALID_ARG
+    assert fwd_keep(keep, need, p=1.0) == b.XFA_ERR_INVALID_ARG
+    assert fwd_keep(keep, need) == b.XFA_ERR_UNSUPPORTED            # the SIMT family keeps no bits
+    p9 = [ctypes.c_void_p(4096 * (i + 1)) for i in range(9)]
+    ws = lib.xfa_bwd_workspace_bytes(1, 8, 64, b.XFA_BF16)
+
+    def bwd_keep(buf, nbytes, impl=b.IMPL_SIMT):
+        return lib.xfa_bwd_dropout_keep(*p9, 1, 8, 64, ctypes.c_float(0.125), b.XFA_BF16, ctypes.c_float(0.1),
+                                        buf, nbytes, ctypes.c_void_p(1 << 24), ws, impl, None)
+
+    assert bwd_keep(None, need) == b.XFA_ERR_INVALID_ARG
+    assert bwd_keep(keep, need - 16) == b.XFA_ERR_INVALID_ARG

@@ -151,3 +151,93 @@ def test_tape_node_with_dropout():
     assert np.array_equal(to_f64(o.value), ref["out"])
     for var, n in ((qv, "dq"), (kv, "dk"), (vv, "dv")):
         assert np.array_equal(to_f64(var.grad), ref[n]), n
+
+
+def _keep_pair(x, dtype, hd, p, seed, impl=2):
+    """Forward + backward with the keep-bit cache, and the re-drawing pair on the same inputs."""
+    from bwd_xfa_fwd_gb300 import binding
+    q, k, v, do = (to_device(x[n], dtype) for n in ("q", "k", "v", "dout"))
+    bh, S, _ = q.shape
+    scale = 1.0 / math.sqrt(hd)
+    keep = torch.full((binding.dropout_keep_bytes(bh, S),), 0xAB, device="cuda", dtype=torch.uint8)
+    out_k, lse_k = binding.fwd(q, k, v, scale, impl, dropout_p=p, seed=seed, keep_bits=keep)
+    g_k = binding.bwd(q, k, v, out_k, do, lse_k, scale, impl, dropout_p=p, keep_bits=keep)
+    out_d, lse_d = binding.fwd(q, k, v, scale, impl, dropout_p=p, seed=seed)
+    g_d = binding.bwd(q, k, v, out_d, do, lse_d, scale, impl, dropout_p=p, seed=seed)
+    torch.cuda.synchronize()
+    assert binding.status() == binding.XFA_OK
+    return keep, (out_k, lse_k) + tuple(g_k), (out_d, lse_d) + tuple(g_d)
+
+
+def _assert_same_as_redrawn(cached, redrawn):
+    """Forward, dK and dV bit for bit; dQ is summed with reduce-adds in a data-dependent
+    order, so two runs of the same backward differ by bf16 rounding steps."""
+    for name, a, b in zip(("out", "lse", "dq", "dk", "dv"), cached, redrawn):
+        if name == "dq":
+            tol = 1e-2 * float(b.float().abs().max())
+            assert torch.allclose(a.float(), b.float(), rtol=0, atol=tol), name
+        else:
+            assert torch.equal(a, b), name
+
+
+@pytest.mark.parametrize("hd", [64, 128])
+@pytest.mark.parametrize("S", [300, 777, 1024])
+def test_cached_keep_bits_give_the_redrawn_results(hd, S):
+    x = inputs.draw((2, S, hd), "bf16", seed=900 + S + hd)
+    _, cached, redrawn = _keep_pair(x, "bf16", hd, 0.2, 0xC0FFEE + S)
+    _assert_same_as_redrawn(cached, redrawn)
+
+
+def test_cached_keep_bits_are_the_oracle_mask():
+    """Decode the forward's keep-bit cache (bit i of word ((b*nkt + kt)*nw + w)*128 + c is
+    the decision of (b, row 32w + i, key 128kt + c)) and compare every decision at or below
+    the diagonal with the oracle's keep()."""
+    bh, S, hd, p, seed = 2, 300, 64, 0.3, 0x1234ABCD5678
+    x = inputs.draw((bh, S, hd), "bf16", seed=31)
+    keep, _, _ = _keep_pair(x, "bf16", hd, p, seed)
+    nkt, nw = (S + 127) // 128, 8 * ((S + 255) // 256)
+    words = keep.view(torch.int32).cpu().numpy().view(np.uint32).reshape(bh, nkt, nw, 128)
+    rows = np.arange(S)
+    bits = (words[:, :, rows // 32, :] >> (rows % 32)[None, None, :, None].astype(np.uint32)) & 1   # [b, kt, row, c]
+    got = bits.transpose(0, 2, 1, 3).reshape(bh, S, nkt * 128)[:, :, :S].astype(bool)
+    want = _kept_reference(bh, S, p, seed)
+    lower = np.tril(np.ones((S, S), dtype=bool))
+    bad = (got != want) & lower
+    assert not bad.any(), f"{int(bad.sum())} cached bits differ, first at {np.argwhere(bad)[0].tolist()}"
+
+
+def test_cached_keep_bits_full_size():
+    """The S = 8192 workload with p = 0.1: the backward from the cache is the re-drawing one."""
+    w = inputs.WORKLOADS[5]
+    x = inputs.workload_inputs(w)
+    _, cached, redrawn = _keep_pair(x, w.dtype, w.hd, 0.1, 2024)
+    _assert_same_as_redrawn(cached, redrawn)
+
+
+def test_cached_keep_bits_rejections():
+    from bwd_xfa_fwd_gb300 import binding
+    x = inputs.draw((1, 256, 64), "bf16", seed=5)
+    q, k, v, do = (to_device(x[n], "bf16") for n in ("q", "k", "v", "dout"))
+    need = binding.dropout_keep_bytes(1, 256)
+    keep = torch.zeros(need, device="cuda", dtype=torch.uint8)
+    with pytest.raises(binding.XfaError) as e:
+        binding.fwd(q, k, v, 0.1, dropout_p=0.2, seed=1, keep_bits=keep[: need - 16])
+    assert e.value.code == binding.XFA_ERR_INVALID_ARG
+    with pytest.raises(binding.XfaError) as e:
+        binding.fwd(q, k, v, 0.1, dropout_p=0.2, seed=1, keep_bits=torch.zeros(need + 4, device="cuda",
+                                                                                 dtype=torch.uint8)[4:])
+    assert e.value.code == binding.XFA_ERR_INVALID_ARG
+    for impl in (binding.IMPL_SIMT,):
+        with pytest.raises(binding.XfaError) as e:
+            binding.fwd(q, k, v, 0.1, impl, dropout_p=0.2, seed=1, keep_bits=keep)
+        assert e.value.code == binding.XFA_ERR_UNSUPPORTED
+    out, lse = binding.fwd(q, k, v, 0.1, dropout_p=0.2, seed=1, keep_bits=keep)
+    for impl in (binding.IMPL_SIMT, binding.IMPL_TCGEN05_DET):
+        with pytest.raises(binding.XfaError) as e:
+            binding.bwd(q, k, v, out, do, lse, 0.1, impl, dropout_p=0.2, keep_bits=keep)
+        assert e.value.code == binding.XFA_ERR_UNSUPPORTED
+    x32 = inputs.draw((1, 256, 64), "f32", seed=5)
+    q32, k32, v32 = (to_device(x32[n], "f32") for n in ("q", "k", "v"))
+    with pytest.raises(binding.XfaError) as e:
+        binding.fwd(q32, k32, v32, 0.1, dropout_p=0.2, seed=1, keep_bits=keep)
+    assert e.value.code == binding.XFA_ERR_UNSUPPORTED
