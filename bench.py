@@ -380,11 +380,12 @@ def run_ours(args, w):
     grads = tuple(torch.empty_like(q) for _ in range(3))
     ws = torch.empty(binding.workspace_bytes(w.bh, w.S, w.hd, q.dtype), device="cuda", dtype=torch.uint8)
     keep = (torch.empty(binding.dropout_keep_bytes(w.bh, w.S), device="cuda", dtype=torch.uint8)
-            if args.dropout and args.keep_bits else None)
+            if args.dropout and args.keep_bits != "none" else None)
     stream = torch.cuda.current_stream()
 
     impl = FAMILIES[args.family]
-    stages = ("fwd", "prep", "main", "finish")
+    fill = bool(args.dropout) and args.keep_bits == "fill"
+    stages = ("fwd", "prep", "main", "finish") + (("keep_fill",) if fill else ())
     K = args.steps
     ev = {s: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
           for s in stages}
@@ -406,13 +407,19 @@ def run_ours(args, w):
             else:
                 mark("finish", 1)
 
+        if fill:
+            # the keep decisions drawn by their own kernel, then read by both attention kernels
+            mark("keep_fill", 0)
+            binding.dropout_keep_fill(w.bh, w.S, args.dropout, DROPOUT_SEED, keep)
+            mark("keep_fill", 1)
         mark("fwd", 0)
         if args.dropout:
             # dropout on the attention probabilities: the backward is one xfa_bwd_dropout call
-            # (its pre-pass, kernel and conversion), timed as "main"; with --keep-bits the pair
-            # caches the forward's keep decisions (xfa_fwd_dropout_keep / xfa_bwd_dropout_keep)
+            # (its pre-pass, kernel and conversion), timed as "main"; with --keep-bits store the forward
+            # caches its keep decisions for the backward (xfa_fwd_dropout_keep / xfa_bwd_dropout_cached),
+            # with --keep-bits fill both read those of xfa_dropout_keep_fill (xfa_fwd_dropout_cached)
             binding.fwd(q, k, v, w.scale, impl, out=out, lse=lse, dropout_p=args.dropout, seed=DROPOUT_SEED,
-                        keep_bits=keep)
+                        keep_bits=keep, keep_cached=fill)
             mark("fwd", 1)
             mark("prep", 0)
             mark("prep", 1)
@@ -492,7 +499,7 @@ def run_ours(args, w):
         "data": data_note(w),
         "config": dict(workload_config(w),
                        **({"dropout_p": args.dropout, "dropout_seed": DROPOUT_SEED} if args.dropout else {}),
-                       **({"dropout_keep_bits": True} if args.dropout and args.keep_bits else {})),
+                       **({"dropout_keep_bits": args.keep_bits} if args.dropout and args.keep_bits != "none" else {})),
         "kernel_family": args.family,
         "fwd_tflops": f_fwd / (per["fwd"] * 1e-3) / 1e12,
         "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
@@ -547,9 +554,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="dropout rate on the attention probabilities (0: none, the benchmark's default)")
-    ap.add_argument("--keep-bits", action="store_true",
-                    help="with --dropout: cache the forward's keep decisions for the backward "
-                         "(xfa_fwd_dropout_keep / xfa_bwd_dropout_keep) instead of drawing them twice")
+    ap.add_argument("--keep-bits", choices=("none", "store", "fill"), default="none", nargs="?", const="store",
+                    help="with --dropout: cache the keep decisions instead of drawing them twice -- 'store': the "
+                         "forward stores them for the backward; 'fill': xfa_dropout_keep_fill draws them (timed "
+                         "as the keep_fill stage) and both kernels read them")
     ap.add_argument("--family", choices=sorted(FAMILIES), default="auto",
                     help="kernel family (xfa_impl): auto, tcgen05 (bf16: dQ by fp32 reductions; fp32 with "
                          "hd 32/64: the 3xTF32 kernels), tcgen05_det (bf16: dQ by a separate pass, "

@@ -48,7 +48,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "xfa_bwd_dropout": ([vp] * 9 + [i, i, i, f, i, f, u64, vp, sz, i, vp], i),
         "xfa_dropout_keep_bytes": ([i, i], sz),
         "xfa_fwd_dropout_keep": ([vp, vp, vp, vp, vp, i, i, i, f, i, f, u64, vp, sz, i, vp], i),
-        "xfa_bwd_dropout_keep": ([vp] * 9 + [i, i, i, f, i, f, vp, sz, vp, sz, i, vp], i),
+        "xfa_fwd_dropout_cached": ([vp, vp, vp, vp, vp, i, i, i, f, i, f, vp, sz, i, vp], i),
+        "xfa_bwd_dropout_cached": ([vp] * 9 + [i, i, i, f, i, f, vp, sz, vp, sz, i, vp], i),
+        "xfa_dropout_keep_fill": ([i, i, f, u64, vp, sz, vp], i),
         "xfa_bwd_prep": ([vp, vp, vp, vp, i, i, i, i, vp, sz, i, vp], i),
         "xfa_bwd_main": ([vp] * 7 + [i, i, i, f, i, vp, sz, i, vp], i),
         "xfa_bwd_finish": ([vp, i, i, i, i, vp, sz, i, vp], i),
@@ -118,19 +120,32 @@ def dropout_keep_bytes(bh: int, S: int) -> int:
     return int(load().xfa_dropout_keep_bytes(bh, S))
 
 
+def dropout_keep_fill(bh: int, S: int, dropout_p: float, seed: int, keep_bits, stream_of=None):
+    """Draw every keep decision of a (bh, S) dropout into ``keep_bits`` (xfa_dropout_keep_fill),
+    on the current stream of ``stream_of``'s device (default: keep_bits')."""
+    ref = keep_bits if stream_of is None else stream_of
+    _check(load().xfa_dropout_keep_fill(bh, S, float(dropout_p), int(seed) % 2 ** 64, _p(keep_bits),
+                                        _nbytes(keep_bits), _stream(ref)), "xfa_dropout_keep_fill")
+
+
 def fwd(q, k, v, scale: float | None = None, impl: int = IMPL_AUTO, out=None, lse=None, dropout_p: float = 0.0,
-        seed: int = 0, keep_bits=None):
+        seed: int = 0, keep_bits=None, keep_cached: bool = False):
     """Forward: returns (O, L).  O has q's shape/dtype; L is fp32 [..., S].  ``dropout_p`` > 0
     applies dropout of that rate to the attention probabilities (xfa_fwd_dropout); the
     backward must get the same ``dropout_p`` and ``seed``.  With ``keep_bits`` (a CUDA uint8
-    tensor of at least :func:`dropout_keep_bytes` bytes) the forward also caches its keep
-    decisions there (xfa_fwd_dropout_keep) for a backward given the same tensor."""
+    tensor of at least :func:`dropout_keep_bytes` bytes) the forward also stores its keep
+    decisions there (xfa_fwd_dropout_keep), or, with ``keep_cached``, reads them from it
+    instead of drawing (xfa_fwd_dropout_cached; filled by :func:`dropout_keep_fill`)."""
     _check_tensors(q, k, v)
     bh, S, hd = _shape3(q)
     scale = default_scale(hd) if scale is None else float(scale)
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty(q.shape[:-1], device=q.device, dtype=torch.float32) if lse is None else lse
-    if dropout_p and keep_bits is not None:
+    if dropout_p and keep_bits is not None and keep_cached:
+        _check(load().xfa_fwd_dropout_cached(_p(q), _p(k), _p(v), _p(out), _p(lse), bh, S, hd, scale,
+                                             _DTYPE[q.dtype], float(dropout_p), _p(keep_bits), _nbytes(keep_bits),
+                                             impl, _stream(q)), "xfa_fwd_dropout_cached")
+    elif dropout_p and keep_bits is not None:
         _check(load().xfa_fwd_dropout_keep(_p(q), _p(k), _p(v), _p(out), _p(lse), bh, S, hd, scale, _DTYPE[q.dtype],
                                            float(dropout_p), int(seed) % 2 ** 64, _p(keep_bits), _nbytes(keep_bits),
                                            impl, _stream(q)), "xfa_fwd_dropout_keep")
@@ -151,8 +166,8 @@ def bwd(q, k, v, out, dout, lse, scale: float | None = None, impl: int = IMPL_AU
         dropout_p: float = 0.0, seed: int = 0, keep_bits=None):
     """Backward: returns (dQ, dK, dV), each of q's shape/dtype (overwritten).  ``dropout_p`` and
     ``seed`` must be those of the forward (xfa_bwd_dropout when ``dropout_p`` > 0); with
-    ``keep_bits``, the forward's cached decisions are read instead of drawn (xfa_bwd_dropout_keep,
-    no seed needed)."""
+    ``keep_bits``, the cached decisions are read instead of drawn (xfa_bwd_dropout_cached, no
+    seed needed)."""
     _check_tensors(q, k, v, out, dout)
     bh, S, hd = _shape3(q)
     scale = default_scale(hd) if scale is None else float(scale)
@@ -161,10 +176,10 @@ def bwd(q, k, v, out, dout, lse, scale: float | None = None, impl: int = IMPL_AU
         workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
     dq, dk, dv = grads if grads is not None else (torch.empty_like(q), torch.empty_like(q), torch.empty_like(q))
     if dropout_p and keep_bits is not None:
-        _check(load().xfa_bwd_dropout_keep(_p(q), _p(k), _p(v), _p(out), _p(dout), _p(lse), _p(dq), _p(dk), _p(dv),
-                                           bh, S, hd, scale, _DTYPE[q.dtype], float(dropout_p), _p(keep_bits),
-                                           _nbytes(keep_bits), _p(workspace), workspace.numel(), impl, _stream(q)),
-               "xfa_bwd_dropout_keep")
+        _check(load().xfa_bwd_dropout_cached(_p(q), _p(k), _p(v), _p(out), _p(dout), _p(lse), _p(dq), _p(dk),
+                                             _p(dv), bh, S, hd, scale, _DTYPE[q.dtype], float(dropout_p),
+                                             _p(keep_bits), _nbytes(keep_bits), _p(workspace), workspace.numel(), impl,
+                                             _stream(q)), "xfa_bwd_dropout_cached")
     elif dropout_p:
         _check(load().xfa_bwd_dropout(_p(q), _p(k), _p(v), _p(out), _p(dout), _p(lse), _p(dq), _p(dk), _p(dv), bh, S,
                                       hd, scale, _DTYPE[q.dtype], float(dropout_p), int(seed) % 2 ** 64,

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libxfa.so")
-SOURCES = ("xfa_api.cu", "aux.cu", "simt.cu", "tc_fwd.cu", "tc_bwd.cu", "tc_dq.cu", "tf_fwd.cu", "tf_bwd.cu", "noalloc.cu")
+SOURCES = ("xfa_api.cu", "aux.cu", "simt.cu", "tc_fwd.cu", "tc_bwd.cu", "tc_dq.cu", "tf_fwd.cu", "tf_bwd.cu", "noalloc.cu", "keep.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -31,10 +31,10 @@ struct DropParams {
     int keep_nkt = 0, keep_w = 0;
 };
 
-// Key tiles (128 keys) and query-row words (32 rows, for the query blocks of 256 rows the
-// forward works in) of the cached keep bits of a [bh, S, S] probability tensor.
+// Key tiles (128 keys) and query-row words (32 rows, four per 128-row query tile) of the cached
+// keep bits of a [bh, S, S] probability tensor.
 inline int keep_key_tiles(int S) { return (S + 127) / 128; }
-inline int keep_row_words(int S) { return 8 * ((S + 255) / 256); }
+inline int keep_row_words(int S) { return 4 * keep_key_tiles(S); }
 inline size_t keep_bits_bytes(int bh, int S)
 {
     return (size_t)bh * (size_t)keep_key_tiles(S) * (size_t)keep_row_words(S) * 128u * 4u;
@@ -95,6 +95,8 @@ cudaError_t launch_rowdot(const void *out, const void *dout, float *d, int bh, i
 cudaError_t launch_convert_dq(const float *acc, void *dq, size_t n, int dtype, cudaStream_t st);
 // dst += src, n elements of dtype.
 cudaError_t launch_accumulate(void *dst, const void *src, size_t n, int dtype, cudaStream_t st);
+// Every cached keep bit at or below the diagonal blocks (keep_word layout) drawn from d.seed.
+cudaError_t launch_keep_fill(const DropParams &d, int bh, int S, uint32_t *keep, cudaStream_t st);
 // A kernel waiting on a barrier nothing arrives on, for at most timeout_us.
 cudaError_t launch_selftest_timeout(unsigned timeout_us, int *status, cudaStream_t st);
 

@@ -410,21 +410,35 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                     for (int t = 0; t < 2; ++t) {
                         if (j >= (t == 0 ? n_t0 : n_t1)) continue;
                         const uint32_t st = nm[t] % MS;
+                        // cached decisions (keep_word: one word per key over this warp's 32 rows), loaded
+                        // before the wait for the stage and turned back into one word per row
+                        const int wrow = (q0 + t * BM + (mw % 4) * 32) / 32;
+                        uint32_t cw[2] = {0u, 0u};
+                        if (drop.keep_in) {
+                            const uint32_t *src = drop.keep_in + keep_word(head, j, wrow, 64 * m + lane, drop.keep_nkt, drop.keep_w);
+                            cw[0] = src[0];
+                            cw[1] = src[32];
+                        }
                         if (nm[t] >= MS &&
                             !(ok = warp_wait(&bars->mask_empty[t][st], ((nm[t] / MS) + 1) & 1, bars, status)))
                             break;
-                        const uint64_t row = (uint64_t)(q0 + t * BM + r);
-                        uint64_t g = (((uint64_t)head * S + row) * (uint64_t)S + (uint64_t)(j * BN + 64 * m)) * kDropGolden;
                         uint32_t w[2];
+                        if (drop.keep_in) {
+                            w[0] = warp_transpose_bits32(cw[0], lane);
+                            w[1] = warp_transpose_bits32(cw[1], lane);
+                        } else {
+                            const uint64_t row = (uint64_t)(q0 + t * BM + r);
+                            uint64_t g = (((uint64_t)head * S + row) * (uint64_t)S + (uint64_t)(j * BN + 64 * m)) * kDropGolden;
 #pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            uint32_t bits = 0u;
+                            for (int q = 0; q < 2; ++q) {
+                                uint32_t bits = 0u;
 #pragma unroll 4
-                            for (int b = 0; b < 32; ++b) {
-                                bits |= (uint32_t)drop_keep(drop.seed, g, drop.keep_thr) << b;
-                                g += kDropGolden;
+                                for (int b = 0; b < 32; ++b) {
+                                    bits |= (uint32_t)drop_keep(drop.seed, g, drop.keep_thr) << b;
+                                    g += kDropGolden;
+                                }
+                                w[q] = bits;
                             }
-                            w[q] = bits;
                         }
                         *reinterpret_cast<uint2 *>(mask_s + ((t * MS + st) * BM + r) * 4 + 2 * m) = make_uint2(w[0], w[1]);
                         __syncwarp();
@@ -433,7 +447,6 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                         if (drop.keep_out) {
                             // the same decisions kept for the backward: one word per key over this
                             // warp's 32 rows (keep_word), 128 contiguous bytes per store
-                            const int wrow = (q0 + t * BM + (mw % 4) * 32) / 32;
                             uint32_t *dst = drop.keep_out + keep_word(head, j, wrow, 64 * m + lane, drop.keep_nkt, drop.keep_w);
                             dst[0] = warp_transpose_bits32(w[0], lane);
                             dst[32] = warp_transpose_bits32(w[1], lane);

@@ -255,7 +255,7 @@ static int fwd_run(const void *q, const void *k, const void *v, void *out, float
     Family fam;
     if ((rc = choose_impl(impl, hd, dtype, &fam)) != XFA_OK) return rc;
     // cached keep bits: the tensor-core bf16 kernels only
-    if (drop.keep_out && fam != Family::TcFused && fam != Family::TcDet) return XFA_ERR_UNSUPPORTED;
+    if ((drop.keep_out || drop.keep_in) && fam != Family::TcFused && fam != Family::TcDet) return XFA_ERR_UNSUPPORTED;
     FwdParams p{q, k, v, out, lse, bh, S, hd, scale, dtype, nullptr};
     p.drop = drop;
     if ((rc = status_ptr(&p.status)) != XFA_OK) return rc;
@@ -297,6 +297,28 @@ int xfa_fwd_dropout_keep(const void *q, const void *k, const void *v, void *out,
     if (rc != XFA_OK || (rc = keep_args(bh, S, keep_bits, keep_bytes, &d)) != XFA_OK) return rc;
     if (d.on) d.keep_out = static_cast<uint32_t *>(keep_bits);
     return fwd_run(q, k, v, out, lse, bh, S, hd, scale, dtype, d, impl, stream);
+}
+
+int xfa_fwd_dropout_cached(const void *q, const void *k, const void *v, void *out, float *lse, int bh, int S,
+                           int hd, float scale, int dtype, float p_drop, const void *keep_bits, size_t keep_bytes,
+                           int impl, void *stream)
+{
+    DropParams d;
+    int rc = make_drop(p_drop, 0, &d);
+    if (rc != XFA_OK || (rc = keep_args(bh, S, keep_bits, keep_bytes, &d)) != XFA_OK) return rc;
+    if (d.on) d.keep_in = static_cast<const uint32_t *>(keep_bits);
+    return fwd_run(q, k, v, out, lse, bh, S, hd, scale, dtype, d, impl, stream);
+}
+
+int xfa_dropout_keep_fill(int bh, int S, float p_drop, unsigned long long seed, void *keep_bits, size_t keep_bytes,
+                          void *stream)
+{
+    DropParams d;
+    int rc = make_drop(p_drop, seed, &d);
+    if (rc != XFA_OK || (rc = keep_args(bh, S, keep_bits, keep_bytes, &d)) != XFA_OK) return rc;
+    if (!d.on) return XFA_OK;   // p_drop == 0: the consumers run the plain kernels and read nothing
+    if (!device_is_sm103()) return XFA_ERR_DEVICE;
+    return cuda_code(launch_keep_fill(d, bh, S, static_cast<uint32_t *>(keep_bits), static_cast<cudaStream_t>(stream)));
 }
 
 int xfa_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int bh, int S, int hd, float scale,
@@ -447,7 +469,7 @@ int xfa_bwd_dropout(const void *q, const void *k, const void *v, const void *out
                    stream);
 }
 
-int xfa_bwd_dropout_keep(const void *q, const void *k, const void *v, const void *out, const void *dout,
+int xfa_bwd_dropout_cached(const void *q, const void *k, const void *v, const void *out, const void *dout,
                          const float *lse, void *dq, void *dk, void *dv, int bh, int S, int hd, float scale,
                          int dtype, float p_drop, const void *keep_bits, size_t keep_bytes, void *workspace,
                          size_t workspace_bytes, int impl, void *stream)

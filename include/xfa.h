@@ -158,38 +158,50 @@ int xfa_bwd_dropout(const void *q, const void *k, const void *v, const void *out
                     void *workspace, size_t workspace_bytes, int impl, void *stream);
 
 /*
- * Dropout with the keep decisions cached between the forward and the backward.  Passage:
- * "xtrain docs/17-dropout.md", sections "Goal" and "Key Design Decisions" (the forward
- * draws the mask and the backward applies that same cached mask).  xfa_fwd_dropout_keep is
- * xfa_fwd_dropout that also writes every decision it draws into keep_bits;
- * xfa_bwd_dropout_keep is xfa_bwd_dropout that reads them from keep_bits instead of drawing
- * them again (the draw is bound by the integer multiplier; a load is not), so it takes no
- * seed.  Results are bit for bit those of the re-drawing calls with the forward's seed.
+ * Dropout with the keep decisions cached in a caller-owned bit buffer.  Passage:
+ * "xtrain docs/17-dropout.md", sections "Goal" and "Key Design Decisions" (the mask is
+ * generated once from (seed, index) and the forward and the backward both apply that same
+ * cached mask).  The draw is bound by the integer multiplier; reading a bit is not.
+ *   xfa_dropout_keep_fill  : draws every decision into keep_bits (a kernel of its own, e.g. on
+ *                            another stream ahead of the attention).
+ *   xfa_fwd_dropout_keep   : xfa_fwd_dropout that also stores every decision it draws.
+ *   xfa_fwd_dropout_cached : xfa_fwd_dropout reading the decisions from keep_bits.
+ *   xfa_bwd_dropout_cached : xfa_bwd_dropout reading the decisions from keep_bits.
+ * The readers take no seed.  Whichever way keep_bits was filled (fill or the storing forward,
+ * with the same bh, S, p_drop and seed), results are bit for bit those of the drawing calls.
  *   keep_bits  : device buffer of at least xfa_dropout_keep_bytes(bh, S) bytes, 16-byte
- *                aligned, owned by the caller; written by the forward, read by the
- *                backward (the same bh, S and p_drop).  Layout: bit i of 32-bit word
+ *                aligned, owned by the caller.  Layout: bit i of 32-bit word
  *                ((b * nkt + kt) * nw + w) * 128 + c is the decision of probability
  *                (b, query row 32 w + i, key 128 kt + c), nkt = ceil(S / 128),
- *                nw = 8 ceil(S / 256); the forward writes the words at or below the
- *                diagonal, the rest stay as they were.
+ *                nw = 4 nkt; the writers write the words with w >= 4 kt (the blocks at
+ *                or below the diagonal, rows and keys past S included), the rest stay as
+ *                they were.
  *   keep_bytes : size of keep_bits in bytes.
  * Families: the tensor-core bf16 kernels (hd 64 / 128; XFA_IMPL_AUTO or XFA_IMPL_TCGEN05,
- * and XFA_IMPL_TCGEN05_DET for the forward); fp32, the SIMT family or XFA_IMPL_TCGEN05_DET in
- * the backward give XFA_ERR_UNSUPPORTED.  p_drop == 0 runs the plain kernels and leaves
- * keep_bits untouched.  A missing, misaligned or short buffer gives XFA_ERR_INVALID_ARG.
+ * and XFA_IMPL_TCGEN05_DET for the forwards); fp32, the SIMT family or XFA_IMPL_TCGEN05_DET in
+ * the backward give XFA_ERR_UNSUPPORTED.  p_drop == 0 runs the plain kernels (the fill does
+ * nothing) and leaves keep_bits untouched.  A missing, misaligned or short buffer gives
+ * XFA_ERR_INVALID_ARG.
  */
 size_t xfa_dropout_keep_bytes(int bh, int S);   /* 0 for bh < 1, S < 1 or a shape no call accepts */
+
+int xfa_dropout_keep_fill(int bh, int S, float p_drop, unsigned long long seed,
+                          void *keep_bits, size_t keep_bytes, void *stream);
 
 int xfa_fwd_dropout_keep(const void *q, const void *k, const void *v, void *out, float *lse,
                          int bh, int S, int hd, float scale, int dtype,
                          float p_drop, unsigned long long seed,
                          void *keep_bits, size_t keep_bytes, int impl, void *stream);
 
-int xfa_bwd_dropout_keep(const void *q, const void *k, const void *v, const void *out, const void *dout,
-                         const float *lse, void *dq, void *dk, void *dv,
-                         int bh, int S, int hd, float scale, int dtype, float p_drop,
-                         const void *keep_bits, size_t keep_bytes,
-                         void *workspace, size_t workspace_bytes, int impl, void *stream);
+int xfa_fwd_dropout_cached(const void *q, const void *k, const void *v, void *out, float *lse,
+                           int bh, int S, int hd, float scale, int dtype, float p_drop,
+                           const void *keep_bits, size_t keep_bytes, int impl, void *stream);
+
+int xfa_bwd_dropout_cached(const void *q, const void *k, const void *v, const void *out, const void *dout,
+                           const float *lse, void *dq, void *dk, void *dv,
+                           int bh, int S, int hd, float scale, int dtype, float p_drop,
+                           const void *keep_bits, size_t keep_bytes,
+                           void *workspace, size_t workspace_bytes, int impl, void *stream);
 
 /*
  * The three stages of xfa_bwd as separate calls, for callers that schedule

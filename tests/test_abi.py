@@ -80,7 +80,7 @@ def test_dropout_keep_bytes_and_validation(lib):
     32, 128 words each) and the host checks of the buffer and of the family."""
     from bwd_xfa_fwd_gb300 import binding as b
     kb = lib.xfa_dropout_keep_bytes
-    assert kb(2, 300) == 2 * 3 * 16 * 128 * 4      # ceil(300/128) key tiles, 8 * ceil(300/256) words
+    assert kb(2, 300) == 2 * 3 * 12 * 128 * 4      # ceil(300/128) key tiles, 4 words of 32 rows each
     assert kb(32, 8192) == 32 * 64 * 256 * 128 * 4
     assert kb(0, 64) == 0 and kb(1, 0) == 0 and kb(1 << 13, 1 << 13) == 0
     good = [ctypes.c_void_p(4096 * (i + 1)) for i in range(5)]
@@ -100,8 +100,11 @@ def test_dropout_keep_bytes_and_validation(lib):
     ws = lib.xfa_bwd_workspace_bytes(1, 8, 64, b.XFA_BF16)
 
     def bwd_keep(buf, nbytes, impl=b.IMPL_SIMT):
-        return lib.xfa_bwd_dropout_keep(*p9, 1, 8, 64, ctypes.c_float(0.125), b.XFA_BF16, ctypes.c_float(0.1),
+        return lib.xfa_bwd_dropout_cached(*p9, 1, 8, 64, ctypes.c_float(0.125), b.XFA_BF16, ctypes.c_float(0.1),
                                         buf, nbytes, ctypes.c_void_p(1 << 24), ws, impl, None)
 
+    assert lib.xfa_dropout_keep_fill(1, 8, ctypes.c_float(0.1), 7, None, need, None) == b.XFA_ERR_INVALID_ARG
+    assert lib.xfa_dropout_keep_fill(1, 8, ctypes.c_float(0.1), 7, keep, need - 4, None) == b.XFA_ERR_INVALID_ARG
+    assert lib.xfa_dropout_keep_fill(1, 8, ctypes.c_float(0.0), 7, keep, need, None) == b.XFA_OK   # nothing to draw
     assert bwd_keep(None, need) == b.XFA_ERR_INVALID_ARG
     assert bwd_keep(keep, need - 16) == b.XFA_ERR_INVALID_ARG

@@ -153,14 +153,18 @@ def test_tape_node_with_dropout():
         assert np.array_equal(to_f64(var.grad), ref[n]), n
 
 
-def _keep_pair(x, dtype, hd, p, seed, impl=2):
-    """Forward + backward with the keep-bit cache, and the re-drawing pair on the same inputs."""
+def _keep_pair(x, dtype, hd, p, seed, impl=2, fill=False):
+    """Forward + backward with the keep-bit cache -- stored by the forward, or (fill) drawn by
+    xfa_dropout_keep_fill and read by both -- and the re-drawing pair on the same inputs."""
     from bwd_xfa_fwd_gb300 import binding
     q, k, v, do = (to_device(x[n], dtype) for n in ("q", "k", "v", "dout"))
     bh, S, _ = q.shape
     scale = 1.0 / math.sqrt(hd)
     keep = torch.full((binding.dropout_keep_bytes(bh, S),), 0xAB, device="cuda", dtype=torch.uint8)
-    out_k, lse_k = binding.fwd(q, k, v, scale, impl, dropout_p=p, seed=seed, keep_bits=keep)
+    if fill:
+        binding.dropout_keep_fill(bh, S, p, seed, keep)
+    out_k, lse_k = binding.fwd(q, k, v, scale, impl, dropout_p=p, seed=0 if fill else seed, keep_bits=keep,
+                               keep_cached=fill)
     g_k = binding.bwd(q, k, v, out_k, do, lse_k, scale, impl, dropout_p=p, keep_bits=keep)
     out_d, lse_d = binding.fwd(q, k, v, scale, impl, dropout_p=p, seed=seed)
     g_d = binding.bwd(q, k, v, out_d, do, lse_d, scale, impl, dropout_p=p, seed=seed)
@@ -180,22 +184,50 @@ def _assert_same_as_redrawn(cached, redrawn):
             assert torch.equal(a, b), name
 
 
+@pytest.mark.parametrize("fill", [False, True])
 @pytest.mark.parametrize("hd", [64, 128])
-@pytest.mark.parametrize("S", [300, 777, 1024])
-def test_cached_keep_bits_give_the_redrawn_results(hd, S):
+@pytest.mark.parametrize("S", [1, 127, 300, 777, 1024])
+def test_cached_keep_bits_give_the_redrawn_results(hd, S, fill):
     x = inputs.draw((2, S, hd), "bf16", seed=900 + S + hd)
-    _, cached, redrawn = _keep_pair(x, "bf16", hd, 0.2, 0xC0FFEE + S)
+    _, cached, redrawn = _keep_pair(x, "bf16", hd, 0.2, 0xC0FFEE + S, fill=fill)
     _assert_same_as_redrawn(cached, redrawn)
+
+
+@pytest.mark.parametrize("S", [1, 200, 300, 777])
+def test_fill_writes_what_the_forward_stores(S):
+    """xfa_dropout_keep_fill and the storing forward write the same bits into every word at or
+    below the diagonal (w >= 4 kt) and leave the others alone."""
+    from bwd_xfa_fwd_gb300 import binding
+    bh, hd, p, seed = 3, 64, 0.25, 0xBADC0DE + S
+    x = inputs.draw((bh, S, hd), "bf16", seed=S)
+    q, k, v = (to_device(x[n], "bf16") for n in ("q", "k", "v"))
+    n = binding.dropout_keep_bytes(bh, S)
+    a = torch.full((n,), 0x5A, device="cuda", dtype=torch.uint8)
+    b = torch.full((n,), 0x5A, device="cuda", dtype=torch.uint8)
+    binding.dropout_keep_fill(bh, S, p, seed, a)
+    binding.fwd(q, k, v, 0.125, dropout_p=p, seed=seed, keep_bits=b)
+    torch.cuda.synchronize()
+    assert binding.status() == binding.XFA_OK
+    nkt = (S + 127) // 128
+    nw = 4 * nkt
+    wa = a.view(torch.int32).reshape(bh, nkt, nw, 128)
+    wb = b.view(torch.int32).reshape(bh, nkt, nw, 128)
+    assert torch.equal(wa, wb)
+    untouched = torch.full((), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+    for kt in range(nkt):
+        assert bool((wa[:, kt, : 4 * kt] == untouched).all()), kt          # above the diagonal: not written
+        assert not bool((wa[:, kt, 4 * kt:] == untouched).all()), kt      # at or below: written
 
 
 def test_cached_keep_bits_are_the_oracle_mask():
     """Decode the forward's keep-bit cache (bit i of word ((b*nkt + kt)*nw + w)*128 + c is
-    the decision of (b, row 32w + i, key 128kt + c)) and compare every decision at or below
-    the diagonal with the oracle's keep()."""
+    the decision of (b, row 32w + i, key 128kt + c), nkt = ceil(S/128), nw = 4 nkt) and compare
+    every decision at or below the diagonal with the oracle's keep()."""
     bh, S, hd, p, seed = 2, 300, 64, 0.3, 0x1234ABCD5678
     x = inputs.draw((bh, S, hd), "bf16", seed=31)
     keep, _, _ = _keep_pair(x, "bf16", hd, p, seed)
-    nkt, nw = (S + 127) // 128, 8 * ((S + 255) // 256)
+    nkt = (S + 127) // 128
+    nw = 4 * nkt
     words = keep.view(torch.int32).cpu().numpy().view(np.uint32).reshape(bh, nkt, nw, 128)
     rows = np.arange(S)
     bits = (words[:, :, rows // 32, :] >> (rows % 32)[None, None, :, None].astype(np.uint32)) & 1   # [b, kt, row, c]
@@ -206,11 +238,12 @@ def test_cached_keep_bits_are_the_oracle_mask():
     assert not bad.any(), f"{int(bad.sum())} cached bits differ, first at {np.argwhere(bad)[0].tolist()}"
 
 
-def test_cached_keep_bits_full_size():
-    """The S = 8192 workload with p = 0.1: the backward from the cache is the re-drawing one."""
+@pytest.mark.parametrize("fill", [False, True])
+def test_cached_keep_bits_full_size(fill):
+    """The S = 8192 workload with p = 0.1: the pair from the cache is the re-drawing one."""
     w = inputs.WORKLOADS[5]
     x = inputs.workload_inputs(w)
-    _, cached, redrawn = _keep_pair(x, w.dtype, w.hd, 0.1, 2024)
+    _, cached, redrawn = _keep_pair(x, w.dtype, w.hd, 0.1, 2024, fill=fill)
     _assert_same_as_redrawn(cached, redrawn)
 
 
@@ -227,10 +260,13 @@ def test_cached_keep_bits_rejections():
         binding.fwd(q, k, v, 0.1, dropout_p=0.2, seed=1, keep_bits=torch.zeros(need + 4, device="cuda",
                                                                                  dtype=torch.uint8)[4:])
     assert e.value.code == binding.XFA_ERR_INVALID_ARG
-    for impl in (binding.IMPL_SIMT,):
+    for cached in (False, True):
         with pytest.raises(binding.XfaError) as e:
-            binding.fwd(q, k, v, 0.1, impl, dropout_p=0.2, seed=1, keep_bits=keep)
+            binding.fwd(q, k, v, 0.1, binding.IMPL_SIMT, dropout_p=0.2, seed=1, keep_bits=keep, keep_cached=cached)
         assert e.value.code == binding.XFA_ERR_UNSUPPORTED
+    with pytest.raises(binding.XfaError) as e:
+        binding.dropout_keep_fill(1, 256, 0.2, 1, keep[: need - 16])
+    assert e.value.code == binding.XFA_ERR_INVALID_ARG
     out, lse = binding.fwd(q, k, v, 0.1, dropout_p=0.2, seed=1, keep_bits=keep)
     for impl in (binding.IMPL_SIMT, binding.IMPL_TCGEN05_DET):
         with pytest.raises(binding.XfaError) as e:
