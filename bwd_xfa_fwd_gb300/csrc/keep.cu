@@ -16,24 +16,25 @@
 namespace xfa {
 namespace {
 
-// Block = (b, kt): 128 keys x 4 word rows per step; thread = key c, word rows w = 4 kt + y, + 4, ...
+// Block = (b, kt) x a chunk of 4 word rows: thread = one word (key c, word row w = 4 chunk + y),
+// 32 draws; chunks wholly above the diagonal block exit at once.  Every block does the same work,
+// so the grid has no tail of long blocks.
 __global__ void __launch_bounds__(512) keep_fill_kernel(uint32_t *__restrict__ keep, int S, int nkt, int nw,
                                                         uint64_t seed, uint32_t keep_thr)
 {
     const int b = (int)blockIdx.x / nkt, kt = (int)blockIdx.x % nkt;
-    const int c = threadIdx.x, y = threadIdx.y;
+    const int w = 4 * (int)blockIdx.y + (int)threadIdx.y, c = threadIdx.x;
+    if (4 * (int)blockIdx.y < 4 * kt || w >= nw) return;
     const uint64_t key = (uint64_t)(kt * 128 + c);
     const uint64_t step = (uint64_t)S * kDropGolden;   // the next row, same key
-    for (int w = 4 * kt + y; w < nw; w += blockDim.y) {
-        uint64_t g = (((uint64_t)b * S + 32u * (uint64_t)w) * (uint64_t)S + key) * kDropGolden;
-        uint32_t bits = 0u;
+    uint64_t g = (((uint64_t)b * S + 32u * (uint64_t)w) * (uint64_t)S + key) * kDropGolden;
+    uint32_t bits = 0u;
 #pragma unroll 4
-        for (int i = 0; i < 32; ++i) {
-            bits |= (uint32_t)drop_keep(seed, g, keep_thr) << i;
-            g += step;
-        }
-        keep[keep_word(b, kt, w, c, nkt, nw)] = bits;
+    for (int i = 0; i < 32; ++i) {
+        bits |= (uint32_t)drop_keep(seed, g, keep_thr) << i;
+        g += step;
     }
+    keep[keep_word(b, kt, w, c, nkt, nw)] = bits;
 }
 
 }  // namespace
@@ -41,7 +42,8 @@ __global__ void __launch_bounds__(512) keep_fill_kernel(uint32_t *__restrict__ k
 cudaError_t launch_keep_fill(const DropParams &d, int bh, int S, uint32_t *keep, cudaStream_t st)
 {
     const int nkt = keep_key_tiles(S), nw = keep_row_words(S);
-    keep_fill_kernel<<<(unsigned)(bh * nkt), dim3(128, 4), 0, st>>>(keep, S, nkt, nw, d.seed, d.keep_thr);
+    keep_fill_kernel<<<dim3((unsigned)(bh * nkt), (unsigned)(nw / 4)), dim3(128, 4), 0, st>>>(keep, S, nkt, nw, d.seed,
+                                                                                           d.keep_thr);
     return cudaGetLastError();
 }
 
