@@ -81,24 +81,32 @@ class Var:
 
 
 def flash_attention(q: Var, k: Var, v: Var, scale: Optional[float] = None, impl: int = 0, dropout_p: float = 0.0,
-                    seed: int = 0) -> Var:
+                    seed: int = 0, keep_mask: bool = False) -> Var:
     """Causal flash attention as one tape node: returns Var(O); caches L.  ``dropout_p`` > 0
     drops attention probabilities with the counter-based mask of ``seed``; the backward
-    re-draws the same mask (nothing but the seed is kept)."""
+    re-draws the same mask (nothing but the seed is kept), or, with ``keep_mask`` (bf16
+    tensor-core kernels), reads the mask the forward stored as bits (bh * S^2 / 8 bytes kept
+    with the node) instead of drawing it again."""
     from . import binding
 
-    out, lse = binding.fwd(q.value, k.value, v.value, scale, impl, dropout_p=dropout_p, seed=seed)
+    keep = None
+    if dropout_p and keep_mask:
+        bh, S, _ = binding._shape3(q.value)
+        keep = torch.empty(binding.dropout_keep_bytes(bh, S), device=q.value.device, dtype=torch.uint8)
+    out, lse = binding.fwd(q.value, k.value, v.value, scale, impl, dropout_p=dropout_p, seed=seed, keep_bits=keep)
     hd = q.value.shape[-1]
     sc = binding.default_scale(hd) if scale is None else float(scale)
 
     def backward_fn(grad, parents):
         pq, pk, pv = parents
         dq, dk, dv = binding.bwd(pq.value, pk.value, pv.value, out, grad.contiguous(), lse, sc, impl,
-                                 dropout_p=dropout_p, seed=seed)
+                                 dropout_p=dropout_p, seed=seed, keep_bits=keep)
         pq.accumulate(dq)
         pk.accumulate(dk)
         pv.accumulate(dv)
 
     node = Var(out, (q, k, v), backward_fn)
     node.saved["lse"] = lse
+    if keep is not None:
+        node.saved["keep_bits"] = keep
     return node

@@ -277,3 +277,21 @@ def test_cached_keep_bits_rejections():
     with pytest.raises(binding.XfaError) as e:
         binding.fwd(q32, k32, v32, 0.1, dropout_p=0.2, seed=1, keep_bits=keep)
     assert e.value.code == binding.XFA_ERR_UNSUPPORTED
+
+
+def test_tape_node_with_a_kept_mask():
+    """The tape node with keep_mask: the forward stores its mask, the backward reads it; the
+    results are the re-drawing node's (dQ up to the order of its reduce-adds)."""
+    from bwd_xfa_fwd_gb300 import binding, tape
+    x = inputs.draw((2, 300, 128), "bf16", seed=22)
+    dev = {n: to_device(x[n], "bf16") for n in ("q", "k", "v", "dout")}
+    res = []
+    for keep_mask in (False, True):
+        qv, kv, vv = (tape.Var(dev[n].clone()) for n in ("q", "k", "v"))
+        o = tape.flash_attention(qv, kv, vv, dropout_p=0.25, seed=78, keep_mask=keep_mask)
+        assert ("keep_bits" in o.saved) == keep_mask
+        o.backward(seed=dev["dout"])
+        torch.cuda.synchronize()
+        assert binding.status() == binding.XFA_OK
+        res.append((o.value, o.saved["lse"], qv.grad, kv.grad, vv.grad))
+    _assert_same_as_redrawn(res[1], res[0])
