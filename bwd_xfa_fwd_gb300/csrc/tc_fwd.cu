@@ -167,7 +167,9 @@ __device__ __forceinline__ void load_scores_half(uint32_t tS, int h, bool diag, 
 }
 
 // DROP: dropout on the probabilities that enter P.V (the row sums l keep every p).
-template <int HD, bool DROP>
+// KEEP (with DROP): the keep bits are read from the cache (DropParams::keep_in) instead of drawn;
+// the keep-bit warps then need few registers and the softmax warps get more.
+template <int HD, bool DROP, bool KEEP = false>
 __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ O,
@@ -387,7 +389,10 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
         }
     } else if (warp >= 12) {
         if (DROP) {
-            regs_decrease<56>();
+            if (KEEP)
+                regs_decrease<32>();
+            else
+                regs_decrease<56>();
             // keep bits (dropout): thread = row r of both tiles, half m of the keys; for every key
             // tile of the item, in the order the softmax groups consume them, the 64 decisions of
             // the row's keys 64m..64m+63 as two 32-bit words, element (row, key) drawn from its flat
@@ -414,7 +419,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                         // before the wait for the stage and turned back into one word per row
                         const int wrow = (q0 + t * BM + (mw % 4) * 32) / 32;
                         uint32_t cw[2] = {0u, 0u};
-                        if (drop.keep_in) {
+                        if (KEEP) {
                             const uint32_t *src = drop.keep_in + keep_word(head, j, wrow, 64 * m + lane, drop.keep_nkt, drop.keep_w);
                             cw[0] = src[0];
                             cw[1] = src[32];
@@ -423,7 +428,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                             !(ok = warp_wait(&bars->mask_empty[t][st], ((nm[t] / MS) + 1) & 1, bars, status)))
                             break;
                         uint32_t w[2];
-                        if (drop.keep_in) {
+                        if (KEEP) {
                             w[0] = warp_transpose_bits32(cw[0], lane);
                             w[1] = warp_transpose_bits32(cw[1], lane);
                         } else {
@@ -444,7 +449,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&bars->mask_full[t][st]);
                         ++nm[t];
-                        if (drop.keep_out) {
+                        if (!KEEP && drop.keep_out) {
                             // the same decisions kept for the backward: one word per key over this
                             // warp's 32 rows (keep_word), 128 contiguous bytes per store
                             uint32_t *dst = drop.keep_out + keep_word(head, j, wrow, 64 * m + lane, drop.keep_nkt, drop.keep_w);
@@ -456,7 +461,14 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
             }
         }
     } else {
-        if (DROP) regs_increase<152>();
+        // 640 threads x 96 registers: per lane of a warpgroup 2 x 152 + 56 + 2 x 56 = 472 (drawing),
+        // 2 x 176 + 56 + 2 x 32 = 472 (reading the cache), within 5 x 96 = 480
+        if (DROP) {
+            if (KEEP)
+                regs_increase<176>();
+            else
+                regs_increase<152>();
+        }
         // softmax group of tile t; thread = query row
         const int t = warp / 4, wq = warp % 4;
         const int r = wq * 32 + lane;               // row within the tile == TMEM lane
@@ -651,7 +663,7 @@ int next_item_counter(cudaStream_t st, unsigned **ctr)
     return XFA_OK;
 }
 
-template <int HD, bool DROP>
+template <int HD, bool DROP, bool KEEP = false>
 int run(const FwdParams &p, cudaStream_t st)
 {
     alignas(64) CUtensorMap tq, tk, tv;
@@ -661,7 +673,7 @@ int run(const FwdParams &p, cudaStream_t st)
     if (rc != XFA_OK) return rc;
     constexpr int smem = Cfg<HD>::template smem<DROP>();
     static_assert(smem <= 227 * 1024, "shared memory per CTA");
-    auto kern = tc_fwd_kernel<HD, DROP>;
+    auto kern = tc_fwd_kernel<HD, DROP, KEEP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return XFA_ERR_CUDA_BASE + (int)e;
     const int nqb = (p.S + 2 * BM - 1) / (2 * BM);
@@ -680,8 +692,14 @@ int run(const FwdParams &p, cudaStream_t st)
 int launch_tc_fwd(const FwdParams &p, cudaStream_t st)
 {
     if (p.dtype != XFA_BF16) return XFA_ERR_UNSUPPORTED;
-    if (p.hd == 128) return p.drop.on ? run<128, true>(p, st) : run<128, false>(p, st);
-    if (p.hd == 64) return p.drop.on ? run<64, true>(p, st) : run<64, false>(p, st);
+    if (p.hd == 128) {
+        if (p.drop.on) return p.drop.keep_in ? run<128, true, true>(p, st) : run<128, true>(p, st);
+        return run<128, false>(p, st);
+    }
+    if (p.hd == 64) {
+        if (p.drop.on) return p.drop.keep_in ? run<64, true, true>(p, st) : run<64, true>(p, st);
+        return run<64, false>(p, st);
+    }
     return XFA_ERR_UNSUPPORTED;
 }
 
