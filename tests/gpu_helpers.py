@@ -26,15 +26,24 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def run_gpu(x, dtype: str, scale: float, impl: int = 0, backward: bool = True, dropout=None):
-    """``dropout = (p, seed)``: dropout on the attention probabilities."""
+def run_gpu(x, dtype: str, scale: float, impl: int = 0, backward: bool = True, dropout=None, keep: str = "none"):
+    """``dropout = (p, seed)``: dropout on the attention probabilities.  ``keep``: "none" (both
+    kernels draw the mask), "store" (the forward stores it as bits, the backward reads them) or
+    "fill" (xfa_dropout_keep_fill draws it, both kernels read it)."""
     from bwd_xfa_fwd_gb300 import binding
     p_drop, seed = (0.0, 0) if dropout is None else dropout
     q, k, v, do = (to_device(x[n], dtype) for n in ("q", "k", "v", "dout"))
-    out, lse = binding.fwd(q, k, v, scale, impl, dropout_p=p_drop, seed=seed)
+    bits = None
+    if p_drop and keep != "none":
+        bh, S = q.shape[0], q.shape[1]
+        bits = torch.full((binding.dropout_keep_bytes(bh, S),), 0xCD, device=q.device, dtype=torch.uint8)
+        if keep == "fill":
+            binding.dropout_keep_fill(bh, S, p_drop, seed, bits)
+    out, lse = binding.fwd(q, k, v, scale, impl, dropout_p=p_drop, seed=seed, keep_bits=bits,
+                           keep_cached=keep == "fill")
     res = {"out": out, "lse": lse}
     if backward:
-        dq, dk, dv = binding.bwd(q, k, v, out, do, lse, scale, impl, dropout_p=p_drop, seed=seed)
+        dq, dk, dv = binding.bwd(q, k, v, out, do, lse, scale, impl, dropout_p=p_drop, seed=seed, keep_bits=bits)
         res.update(dq=dq, dk=dk, dv=dv)
     torch.cuda.synchronize()
     assert binding.status() == binding.XFA_OK

@@ -266,6 +266,7 @@ def _fuzz_cases(n=int(os.environ.get("XFA_FUZZ_CASES", "24")), seed=2024):
     rng = np.random.default_rng(seed)
     rng_drop = np.random.default_rng(seed + 1)
     rng_f32 = np.random.default_rng(seed + 2)   # fp32 kernel family
+    rng_keep = np.random.default_rng(seed + 3)  # how the dropout mask travels (bf16 tensor cores)
     cases = []
     for i in range(n):
         dtype = "bf16" if i % 4 else "f32"
@@ -276,16 +277,18 @@ def _fuzz_cases(n=int(os.environ.get("XFA_FUZZ_CASES", "24")), seed=2024):
         scale = float(rng.uniform(0.02, 0.3))
         std = float(rng.choice([0.5, 1.0, 2.0, 3.0]))
         p_drop = float(rng_drop.choice([0.0, 0.0, 0.1, 0.3])) if (dtype, impl) != ("bf16", 3) else 0.0
-        cases.append((i, dtype, hd, impl, S, bh, scale, std, p_drop))
+        keep = str(rng_keep.choice(["none", "store", "fill"])) if p_drop and dtype == "bf16" else "none"
+        cases.append((i, dtype, hd, impl, S, bh, scale, std, p_drop, keep))
     return cases
 
 
 @pytest.mark.parametrize("case", _fuzz_cases(),
-                         ids=lambda c: f"{c[0]}-{c[1]}-hd{c[2]}-impl{c[3]}-S{c[4]}-bh{c[5]}-p{c[8]}")
+                         ids=lambda c: f"{c[0]}-{c[1]}-hd{c[2]}-impl{c[3]}-S{c[4]}-bh{c[5]}-p{c[8]}-{c[9]}")
 def test_random_shapes_against_oracle(case):
-    """Seeded random shapes, scales, input spreads, kernel families and dropout rates."""
-    i, dtype, hd, impl, S, bh, scale, std, p_drop = case
+    """Seeded random shapes, scales, input spreads, kernel families, dropout rates and ways
+    of carrying the dropout mask (drawn twice, stored by the forward, or filled ahead)."""
+    i, dtype, hd, impl, S, bh, scale, std, p_drop, keep = case
     x = inputs.draw((bh, S, hd), dtype, seed=7000 + i, stds=(std, std, 1.0, 1.0))
     drop = (p_drop, 9000 + i) if p_drop else None
-    got = run_gpu(x, dtype, scale, impl=impl, dropout=drop)
+    got = run_gpu(x, dtype, scale, impl=impl, dropout=drop, keep=keep)
     compare(got, oracle_result(("fuzz", i), x, scale, dropout=drop), dtype)
