@@ -156,3 +156,50 @@ def test_graph_replays_overlapping_eager_launches():
     for o in eager_outs:
         for a, b in zip(cases[1]["ref"], o):
             assert torch.equal(a, b)
+
+
+def test_graph_replays_the_cached_dropout_step():
+    """The dropout step with its mask drawn by its own kernel and read by both attention kernels
+    (xfa_dropout_keep_fill, xfa_fwd_dropout_cached, xfa_bwd_dropout_cached) captured once and
+    replayed: every replay gives the eager results (dQ up to the order of its reduce-adds)."""
+    from bwd_xfa_fwd_gb300 import binding
+    bh, S, hd, p, seed = 3, 700, 128, 0.15, 0xD00D
+    scale = 1.0 / math.sqrt(hd)
+    x = inputs.draw((bh, S, hd), "bf16", seed=91)
+    q, k, v, do = (to_device(x[n], "bf16") for n in ("q", "k", "v", "dout"))
+    out = torch.empty_like(q)
+    lse = torch.empty(bh, S, device="cuda", dtype=torch.float32)
+    grads = tuple(torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(binding.workspace_bytes(bh, S, hd, q.dtype), device="cuda", dtype=torch.uint8)
+    keep = torch.empty(binding.dropout_keep_bytes(bh, S), device="cuda", dtype=torch.uint8)
+
+    def step():
+        binding.dropout_keep_fill(bh, S, p, seed, keep, stream_of=q)
+        binding.fwd(q, k, v, scale, out=out, lse=lse, dropout_p=p, keep_bits=keep, keep_cached=True)
+        binding.bwd(q, k, v, out, do, lse, scale, workspace=ws, grads=grads, dropout_p=p, keep_bits=keep)
+
+    step()
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in (out, lse) + grads]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(2):
+        for t in (out, lse) + grads:
+            t.fill_(float("nan"))
+        keep.fill_(0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert binding.status() == binding.XFA_OK
+        for name, a, b in zip(("out", "lse", "dq", "dk", "dv"), eager, (out, lse) + grads):
+            if name == "dq":
+                tol = 1e-2 * float(a.float().abs().max())
+                assert torch.allclose(a.float(), b.float(), rtol=0, atol=tol), name
+            else:
+                assert torch.equal(a, b), name
