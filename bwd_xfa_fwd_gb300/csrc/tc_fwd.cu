@@ -62,6 +62,10 @@ struct Cfg {
     static constexpr int SUB_BYTES = 128 * 128;         // 128 rows x 128 B
     static constexpr int TILE_BYTES = BM * HD * 2;      // BM == BN
     static constexpr int NS = HD == 128 ? 2 : 3;        // K/V ring depth
+    // hd = 64: one barrier for a key tile's K and V (k_full on arrival, v_empty on release), one
+    // wait per key step instead of two; hd = 128 keeps separate ones, since with its two-stage ring
+    // K's stage must be freed as soon as S has read it (holding it until P.V measured 20 % slower)
+    static constexpr bool KV1 = HD == 64;
     static constexpr int OFF_Q0 = 0;
     static constexpr int OFF_Q1 = TILE_BYTES;
     static constexpr int OFF_K = 2 * TILE_BYTES;
@@ -278,16 +282,20 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                     for (int j = 0; j < nkv; ++j, ++g) {
                         const int st = g % C::NS;
                         const uint32_t ph = ((g / C::NS) + 1) & 1;   // parity of the release of the previous use
-                        if (g >= C::NS && !(ok = mbar_wait_spin(&bars->k_empty[st], ph, &bars->abort))) break;
-                        mbar_arrive_expect_tx(&bars->k_full[st], C::TILE_BYTES);
+                        if (g >= C::NS && !(ok = mbar_wait_spin(C::KV1 ? &bars->v_empty[st] : &bars->k_empty[st], ph, &bars->abort)))
+                            break;
+                        mbar_arrive_expect_tx(&bars->k_full[st], (C::KV1 ? 2 : 1) * C::TILE_BYTES);
                         for (int s = 0; s < C::SUB; ++s)
                             tma_load_3d(smem + C::OFF_K + st * C::TILE_BYTES + s * C::SUB_BYTES, &tm_k, &bars->k_full[st],
                                         s * 64, j * BN, head);
                         last_k[st] = g + 1;
-                        if (g >= C::NS && !(ok = mbar_wait_spin(&bars->v_empty[st], ph, &bars->abort))) break;
-                        mbar_arrive_expect_tx(&bars->v_full[st], C::TILE_BYTES);
+                        if (!C::KV1) {
+                            if (g >= C::NS && !(ok = mbar_wait_spin(&bars->v_empty[st], ph, &bars->abort))) break;
+                            mbar_arrive_expect_tx(&bars->v_full[st], C::TILE_BYTES);
+                        }
                         for (int s = 0; s < C::SUB; ++s)
-                            tma_load_3d(smem + C::OFF_V + st * C::TILE_BYTES + s * C::SUB_BYTES, &tm_v, &bars->v_full[st],
+                            tma_load_3d(smem + C::OFF_V + st * C::TILE_BYTES + s * C::SUB_BYTES, &tm_v,
+                                        C::KV1 ? &bars->k_full[st] : &bars->v_full[st],
                                         s * 64, j * BN, head);
                         last_v[st] = g + 1;
                     }
@@ -297,7 +305,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                 if (k > 0) mbar_wait_spin(&bars->q_full, (k - 1) & 1, nullptr);
                 for (int st = 0; st < C::NS; ++st) {
                     if (last_k[st]) mbar_wait_spin(&bars->k_full[st], ((last_k[st] - 1) / C::NS) & 1, nullptr);
-                    if (last_v[st]) mbar_wait_spin(&bars->v_full[st], ((last_v[st] - 1) / C::NS) & 1, nullptr);
+                    if (!C::KV1 && last_v[st]) mbar_wait_spin(&bars->v_full[st], ((last_v[st] - 1) / C::NS) & 1, nullptr);
                 }
             }
         } else if (warp == kWarpMma) {
@@ -335,7 +343,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                         issue_qk<HD>(tmem + C::col_s(1), q_desc[1], sdesc_advance(k_desc, st0 * C::TILE_BYTES));
                         tc_commit(&bars->s_full[1]);
                     }
-                    tc_commit(&bars->k_empty[st0]);
+                    if (!C::KV1) tc_commit(&bars->k_empty[st0]);
                     if (nkv == 1) tc_commit(&bars->q_empty);   // no further S of this item reads Q
                 }
                 __syncwarp();
@@ -351,7 +359,8 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                         if (j >= nt) continue;
                         ok = warp_wait(&bars->p_full[t], np[t] & 1, bars, status);
                         ++np[t];
-                        if (ok && !v_ready) ok = v_ready = warp_wait(&bars->v_full[st], ph, bars, status);
+                        // (KV1: V arrived with K, waited for before this key tile's S)
+                        if (ok && !v_ready) ok = v_ready = C::KV1 || warp_wait(&bars->v_full[st], ph, bars, status);
                         if (!ok) break;
                         tc_fence_after_sync();
                         if (leader) {
@@ -373,7 +382,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                     }
                     if (!ok) break;
                     if (leader) {
-                        if (k_next_ready) tc_commit(&bars->k_empty[stn]);
+                        if (!C::KV1 && k_next_ready) tc_commit(&bars->k_empty[stn]);
                         tc_commit(&bars->v_empty[st]);
                         if (jn == nkv - 1) tc_commit(&bars->q_empty);   // the item's last S MMAs are issued
                     }
