@@ -62,10 +62,6 @@ struct Cfg {
     static constexpr int SUB_BYTES = 128 * 128;         // 128 rows x 128 B
     static constexpr int TILE_BYTES = BM * HD * 2;      // BM == BN
     static constexpr int NS = HD == 128 ? 2 : 3;        // K/V ring depth
-    // hd = 64: one barrier for a key tile's K and V (k_full on arrival, v_empty on release), one
-    // wait per key step instead of two; hd = 128 keeps separate ones, since with its two-stage ring
-    // K's stage must be freed as soon as S has read it (holding it until P.V measured 20 % slower)
-    static constexpr bool KV1 = HD == 64;
     static constexpr int OFF_Q0 = 0;
     static constexpr int OFF_Q1 = TILE_BYTES;
     static constexpr int OFF_K = 2 * TILE_BYTES;
@@ -255,58 +251,97 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                 prefetch_tensormap(&tm_k);
                 prefetch_tensormap(&tm_v);
                 uint32_t g = 0;                       // K/V tiles issued by this CTA
-                uint32_t last_k[3] = {0, 0, 0}, last_v[3] = {0, 0, 0};   // 1 + last tile issued per stage
+                uint32_t last_v[3] = {0, 0, 0};      // 1 + last tile whose V (and the next K) went to each stage
                 int k = 0;                            // items whose Q was issued
+                int kc = 0;                           // items claimed, posted in ring entry kc & 1
                 bool ok = true;
-                for (int kc = 0; ok; ++kc) {          // kc: items claimed, posted in ring entry kc & 1
+                // Claim the next work item and post its id to the other warps (-1: no more work).
+                auto claim = [&]() -> int {
                     const int e = kc & 1;
-                    if (kc >= 2 && !(ok = mbar_wait_spin(&bars->item_empty[e], ((kc >> 1) + 1) & 1, &bars->abort))) break;
-                    int item = (int)atomicAdd(next_item, 1u);
-                    if (item >= n_items) item = -1;
-                    *reinterpret_cast<volatile int *>(&bars->item_id[e]) = item;
+                    if (kc >= 2 && !(ok = mbar_wait_spin(&bars->item_empty[e], ((kc >> 1) + 1) & 1, &bars->abort)))
+                        return -1;
+                    int it = (int)atomicAdd(next_item, 1u);
+                    if (it >= n_items) it = -1;
+                    *reinterpret_cast<volatile int *>(&bars->item_id[e]) = it;
                     mbar_arrive(&bars->item_full[e]);
-                    if (item < 0) break;
-                    int head, qb;
-                    item_coords(item, head, qb);
-                    const int q0 = qb * 2 * BM;
-                    const bool t1 = q0 + BM < S;
-                    const int nkv = t1 ? 2 * qb + 2 : 2 * qb + 1;
-                    // the Q buffers are free once the previous item's last S MMAs have read them
-                    if (k > 0 && !(ok = mbar_wait_spin(&bars->q_empty, (k - 1) & 1, &bars->abort))) break;
+                    ++kc;
+                    return it;
+                };
+                // Q of an item: the Q buffers are free once the previous item's last S MMAs have read them.
+                auto load_q = [&](int head, int q0, bool t1) {
+                    if (k > 0 && !(ok = mbar_wait_spin(&bars->q_empty, (k - 1) & 1, &bars->abort))) return;
                     mbar_arrive_expect_tx(&bars->q_full, (t1 ? 2 : 1) * C::TILE_BYTES);
                     for (int s = 0; s < C::SUB; ++s) {
                         tma_load_3d(smem + C::OFF_Q0 + s * C::SUB_BYTES, &tm_q, &bars->q_full, s * 64, q0, head);
                         if (t1) tma_load_3d(smem + C::OFF_Q1 + s * C::SUB_BYTES, &tm_q, &bars->q_full, s * 64, q0 + BM, head);
                     }
                     ++k;
-                    for (int j = 0; j < nkv; ++j, ++g) {
+                };
+                // K of the CTA's tile gk (key tile j of `head`) into its stage, completing on `bar`; the stage is
+                // free once the S MMAs of tile gk - NS have read it.
+                auto load_k = [&](uint32_t gk, int head, int j, uint64_t *bar) {
+                    const int st = gk % C::NS;
+                    if (gk >= C::NS && !(ok = mbar_wait_spin(&bars->k_empty[st], ((gk / C::NS) + 1) & 1, &bars->abort)))
+                        return;
+                    for (int s = 0; s < C::SUB; ++s)
+                        tma_load_3d(smem + C::OFF_K + st * C::TILE_BYTES + s * C::SUB_BYTES, &tm_k, bar, s * 64, j * BN, head);
+                };
+                // V of tile g and K of tile g + 1 (the next key tile of the item, or the next item's first)
+                // complete on one barrier, v_full[g % NS]: the MMA warp waits once per key step.  The CTA's
+                // first K completes on k_full[0].
+                bool k0 = false;
+                int item = claim();
+                if (item >= 0) {
+                    int head, qb;
+                    item_coords(item, head, qb);
+                    int q0 = qb * 2 * BM;
+                    bool t1 = q0 + BM < S;
+                    int nkv = t1 ? 2 * qb + 2 : 2 * qb + 1;
+                    load_q(head, q0, t1);
+                    if (ok) {
+                        mbar_arrive_expect_tx(&bars->k_full[0], C::TILE_BYTES);
+                        load_k(0, head, 0, &bars->k_full[0]);
+                        k0 = true;
+                    }
+                    for (int j = 0; ok;) {
                         const int st = g % C::NS;
-                        const uint32_t ph = ((g / C::NS) + 1) & 1;   // parity of the release of the previous use
-                        if (g >= C::NS && !(ok = mbar_wait_spin(C::KV1 ? &bars->v_empty[st] : &bars->k_empty[st], ph, &bars->abort)))
+                        if (g >= C::NS && !(ok = mbar_wait_spin(&bars->v_empty[st], ((g / C::NS) + 1) & 1, &bars->abort)))
                             break;
-                        mbar_arrive_expect_tx(&bars->k_full[st], (C::KV1 ? 2 : 1) * C::TILE_BYTES);
-                        for (int s = 0; s < C::SUB; ++s)
-                            tma_load_3d(smem + C::OFF_K + st * C::TILE_BYTES + s * C::SUB_BYTES, &tm_k, &bars->k_full[st],
-                                        s * 64, j * BN, head);
-                        last_k[st] = g + 1;
-                        if (!C::KV1) {
-                            if (g >= C::NS && !(ok = mbar_wait_spin(&bars->v_empty[st], ph, &bars->abort))) break;
-                            mbar_arrive_expect_tx(&bars->v_full[st], C::TILE_BYTES);
+                        const bool last = j == nkv - 1;
+                        int nitem = item;
+                        if (last && (nitem = claim()) < 0 && !ok) break;
+                        int nhead = head, nqb = qb, nj = j + 1;
+                        if (last && nitem >= 0) {
+                            item_coords(nitem, nhead, nqb);
+                            nj = 0;
                         }
+                        const bool has_next = !last || nitem >= 0;
+                        mbar_arrive_expect_tx(&bars->v_full[st], (has_next ? 2 : 1) * C::TILE_BYTES);
                         for (int s = 0; s < C::SUB; ++s)
-                            tma_load_3d(smem + C::OFF_V + st * C::TILE_BYTES + s * C::SUB_BYTES, &tm_v,
-                                        C::KV1 ? &bars->k_full[st] : &bars->v_full[st],
+                            tma_load_3d(smem + C::OFF_V + st * C::TILE_BYTES + s * C::SUB_BYTES, &tm_v, &bars->v_full[st],
                                         s * 64, j * BN, head);
                         last_v[st] = g + 1;
+                        if (has_next) load_k(g + 1, nhead, nj, &bars->v_full[st]);
+                        ++g;
+                        if (!ok || !has_next) break;
+                        if (last) {   // on to the next item
+                            item = nitem;
+                            head = nhead;
+                            qb = nqb;
+                            q0 = qb * 2 * BM;
+                            t1 = q0 + BM < S;
+                            nkv = t1 ? 2 * qb + 2 : 2 * qb + 1;
+                            load_q(head, q0, t1);
+                        }
+                        j = nj;
                     }
                 }
                 if (!ok) fail(bars, status);
                 // Never leave the CTA with copies in flight: wait for the last load of Q and of each stage.
                 if (k > 0) mbar_wait_spin(&bars->q_full, (k - 1) & 1, nullptr);
-                for (int st = 0; st < C::NS; ++st) {
-                    if (last_k[st]) mbar_wait_spin(&bars->k_full[st], ((last_k[st] - 1) / C::NS) & 1, nullptr);
-                    if (!C::KV1 && last_v[st]) mbar_wait_spin(&bars->v_full[st], ((last_v[st] - 1) / C::NS) & 1, nullptr);
-                }
+                if (k0) mbar_wait_spin(&bars->k_full[0], 0, nullptr);
+                for (int st = 0; st < C::NS; ++st)
+                    if (last_v[st]) mbar_wait_spin(&bars->v_full[st], ((last_v[st] - 1) / C::NS) & 1, nullptr);
             }
         } else if (warp == kWarpMma) {
             // The whole warp runs the issue loop (converged, so descriptors stay warp-uniform);
@@ -330,8 +365,8 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                 const int n_t0 = 2 * qb + 1, n_t1 = t1 ? 2 * qb + 2 : 0;
                 const int nkv = t1 ? n_t1 : n_t0;
                 const int st0 = g % C::NS;
-                ok = warp_wait(&bars->q_full, k & 1, bars, status) &&
-                     warp_wait(&bars->k_full[st0], (g / C::NS) & 1, bars, status);
+                // the item's first K: the CTA's first on k_full[0], later ones came with the previous V
+                ok = warp_wait(&bars->q_full, k & 1, bars, status) && (g > 0 || warp_wait(&bars->k_full[0], 0, bars, status));
                 if (!ok) break;
                 tc_fence_after_sync();
                 if (leader) {
@@ -343,14 +378,14 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                         issue_qk<HD>(tmem + C::col_s(1), q_desc[1], sdesc_advance(k_desc, st0 * C::TILE_BYTES));
                         tc_commit(&bars->s_full[1]);
                     }
-                    if (!C::KV1) tc_commit(&bars->k_empty[st0]);
+                    tc_commit(&bars->k_empty[st0]);
                     if (nkv == 1) tc_commit(&bars->q_empty);   // no further S of this item reads Q
                 }
                 __syncwarp();
                 for (int j = 0; ok && j < nkv; ++j) {
                     const uint32_t gj = g + j, gn = gj + 1;
                     const int st = gj % C::NS, stn = gn % C::NS;
-                    const uint32_t ph = (gj / C::NS) & 1, phn = (gn / C::NS) & 1;
+                    const uint32_t ph = (gj / C::NS) & 1;
                     bool v_ready = false, k_next_ready = false;
                     const int jn = j + 1;
 #pragma unroll
@@ -359,8 +394,8 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                         if (j >= nt) continue;
                         ok = warp_wait(&bars->p_full[t], np[t] & 1, bars, status);
                         ++np[t];
-                        // (KV1: V arrived with K, waited for before this key tile's S)
-                        if (ok && !v_ready) ok = v_ready = C::KV1 || warp_wait(&bars->v_full[st], ph, bars, status);
+                        // V of this key tile and K of the next arrive together
+                        if (ok && !v_ready) ok = v_ready = warp_wait(&bars->v_full[st], ph, bars, status);
                         if (!ok) break;
                         tc_fence_after_sync();
                         if (leader) {
@@ -370,8 +405,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                         }
                         __syncwarp();
                         if (jn < nt) {
-                            if (!k_next_ready) ok = k_next_ready = warp_wait(&bars->k_full[stn], phn, bars, status);
-                            if (!ok) break;
+                            k_next_ready = true;   // came with this key tile's V
                             tc_fence_after_sync();
                             if (leader) {
                                 issue_qk<HD>(tmem + C::col_s(t), q_desc[t], sdesc_advance(k_desc, stn * C::TILE_BYTES));
@@ -382,7 +416,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                     }
                     if (!ok) break;
                     if (leader) {
-                        if (!C::KV1 && k_next_ready) tc_commit(&bars->k_empty[stn]);
+                        if (k_next_ready) tc_commit(&bars->k_empty[stn]);
                         tc_commit(&bars->v_empty[st]);
                         if (jn == nkv - 1) tc_commit(&bars->q_empty);   // the item's last S MMAs are issued
                     }
