@@ -10,7 +10,9 @@
 //   * persistent CTAs, one per SM; a work item is 256 query rows of one head as two
 //     128-row tiles (t = 0, 1), claimed from a per-launch counter (see the kernel);
 //   * warp 8 claims items and streams Q and the K and V tiles (128 keys x hd) through
-//     a TMA ring with 128-byte swizzle; the ring runs on across items;
+//     a TMA ring with 128-byte swizzle; the ring runs on across items, and the V of
+//     each key tile and the K of the next (in the next item after an item's last)
+//     land on one barrier, so the MMA thread waits once per key step;
 //   * warp 9 (one thread) issues tcgen05.mma: S_t = Q_t K^T into TMEM
 //     (128 lanes x 128 fp32 columns) and O_t += P_t V with P_t read straight
 //     from TMEM (bf16, packed into the first 64 columns of S_t);
@@ -78,6 +80,9 @@ struct Cfg {
 struct Bars {
     uint64_t q_full;
     uint64_t q_empty;     // the item's last S MMAs have read Q (tensor-core commit)
+    // v_full[s]: the V of the key tile in stage s and the K of the next key tile (k_full[0]: the
+    // CTA's first K; the other k_full and v_full's K-only use are not used); k_empty / v_empty: the
+    // stage's K read by its S MMAs / V read by its P.Vs (tensor-core commits)
     uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
     uint64_t s_full[2];   // S_t ready in TMEM (tensor-core commit)
     uint64_t p_full[2];   // P_t written to TMEM (one arrival per softmax warp)
