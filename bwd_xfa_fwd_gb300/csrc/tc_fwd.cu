@@ -80,9 +80,9 @@ struct Cfg {
 struct Bars {
     uint64_t q_full;
     uint64_t q_empty;     // the item's last S MMAs have read Q (tensor-core commit)
-    // v_full[s]: the V of the key tile in stage s and the K of the next key tile (k_full[0]: the
-    // CTA's first K; the other k_full and v_full's K-only use are not used); k_empty / v_empty: the
-    // stage's K read by its S MMAs / V read by its P.Vs (tensor-core commits)
+    // v_full[s]: the V of the key tile in stage s and the K of the next key tile; k_full[0]: the
+    // CTA's first K (k_full[1], k_full[2] are not used); k_empty / v_empty: the stage's K read by
+    // its S MMAs / its V read by its P.Vs (tensor-core commits)
     uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
     uint64_t s_full[2];   // S_t ready in TMEM (tensor-core commit)
     uint64_t p_full[2];   // P_t written to TMEM (one arrival per softmax warp)
