@@ -16,25 +16,33 @@
 namespace xfa {
 namespace {
 
-// Block = (b, kt) x a chunk of 4 word rows: thread = one word (key c, word row w = 4 chunk + y),
-// 32 draws; chunks wholly above the diagonal block exit at once.  Every block does the same work,
-// so the grid has no tail of long blocks.
+// Block = (b, kt) x R chunks of 4 word rows: thread = key c, word row w = 4 chunk + y of each of
+// its R chunks, 32 draws per word; chunks wholly above the diagonal block are skipped.  Large
+// grids take R = 4 (fewer, longer blocks: 4 % faster at bh 32, S 8192), small ones R = 1 (enough
+// blocks to fill the SMs: R = 4 was 10 % slower at bh 96, S 1024).
+template <int kFillChunks>
 __global__ void __launch_bounds__(512) keep_fill_kernel(uint32_t *__restrict__ keep, int S, int nkt, int nw,
                                                         uint64_t seed, uint32_t keep_thr)
 {
     const int b = (int)blockIdx.x / nkt, kt = (int)blockIdx.x % nkt;
-    const int w = 4 * (int)blockIdx.y + (int)threadIdx.y, c = threadIdx.x;
-    if (4 * (int)blockIdx.y < 4 * kt || w >= nw) return;
+    const int chunk0 = kFillChunks * (int)blockIdx.y, c = threadIdx.x;
+    if (chunk0 + kFillChunks <= kt) return;
     const uint64_t key = (uint64_t)(kt * 128 + c);
     const uint64_t step = (uint64_t)S * kDropGolden;   // the next row, same key
-    uint64_t g = (((uint64_t)b * S + 32u * (uint64_t)w) * (uint64_t)S + key) * kDropGolden;
-    uint32_t bits = 0u;
+#pragma unroll 1
+    for (int r = 0; r < kFillChunks; ++r) {
+        const int chunk = chunk0 + r;
+        if (chunk < kt || chunk >= nkt) continue;
+        const int w = 4 * chunk + (int)threadIdx.y;
+        uint64_t g = (((uint64_t)b * S + 32u * (uint64_t)w) * (uint64_t)S + key) * kDropGolden;
+        uint32_t bits = 0u;
 #pragma unroll 4
-    for (int i = 0; i < 32; ++i) {
-        bits |= (uint32_t)drop_keep(seed, g, keep_thr) << i;
-        g += step;
+        for (int i = 0; i < 32; ++i) {
+            bits |= (uint32_t)drop_keep(seed, g, keep_thr) << i;
+            g += step;
+        }
+        keep[keep_word(b, kt, w, c, nkt, nw)] = bits;
     }
-    keep[keep_word(b, kt, w, c, nkt, nw)] = bits;
 }
 
 }  // namespace
@@ -42,8 +50,13 @@ __global__ void __launch_bounds__(512) keep_fill_kernel(uint32_t *__restrict__ k
 cudaError_t launch_keep_fill(const DropParams &d, int bh, int S, uint32_t *keep, cudaStream_t st)
 {
     const int nkt = keep_key_tiles(S), nw = keep_row_words(S);
-    keep_fill_kernel<<<dim3((unsigned)(bh * nkt), (unsigned)(nw / 4)), dim3(128, 4), 0, st>>>(keep, S, nkt, nw, d.seed,
-                                                                                           d.keep_thr);
+    const bool large = (long long)bh * nkt * nkt >= 40000;
+    if (large)
+        keep_fill_kernel<4><<<dim3((unsigned)(bh * nkt), (unsigned)((nkt + 3) / 4)), dim3(128, 4), 0, st>>>(
+            keep, S, nkt, nw, d.seed, d.keep_thr);
+    else
+        keep_fill_kernel<1><<<dim3((unsigned)(bh * nkt), (unsigned)nkt), dim3(128, 4), 0, st>>>(keep, S, nkt, nw, d.seed,
+                                                                                             d.keep_thr);
     return cudaGetLastError();
 }
 
