@@ -43,13 +43,15 @@ constexpr int BM = 128;               // query rows per tile (MMA M)
 constexpr int BN = 128;               // keys per tile (MMA N of S, K of P.V)
 constexpr int kThreads = 320;         // 10 warps
 constexpr int kWarpTma = 8, kWarpMma = 9;
-// With dropout: 20 warps.  Warps 12-19 (two warpgroups, two warps per SM sub-partition: the draw
-// is bound by the integer multiplier, which one warp per sub-partition does not keep busy) draw
-// the keep bits of every (row, key) of the coming key tiles into shared memory (MS stages per
-// tile), so the softmax warps only read them; warps 10-11 are idle.  A 640-thread launch gets 96
-// registers a thread; they move from the TMA/MMA/idle warpgroup and the mask warpgroups to the
-// softmax warpgroups: 2 x 152 + 56 + 2 x 56 = 480 per lane of a warpgroup, 96 x 5.
-constexpr int kMaskWarps = 8;
+// With dropout: 28 warps.  Warps 12-27 (four warpgroups, four warps per SM sub-partition: the draw
+// is bound by the integer multiplier, which it shares with the softmax's fp32 arithmetic, and
+// more warps keep more draws in flight: 16 warps measured 3-4 % faster than 8, 8 than 4) draw the
+// keep bits of every (row, key) of the coming key tiles into shared memory (MS stages per tile),
+// one 32-key word per thread, so the softmax warps only read them; warps 10-11 are idle.  An
+// 896-thread launch gets 72 registers a thread; they move from the TMA/MMA/idle warpgroup and
+// the keep-bit warpgroups to the softmax warpgroups (the counts at the softmax's setmaxnreg).
+constexpr int kMaskWarps = 16;
+constexpr int kMaskWords = 16 / kMaskWarps;   // 32-key words of a row per keep-bit thread
 constexpr int kWarpMask0 = 12;
 constexpr int kThreadsDrop = (kWarpMask0 + kMaskWarps) * 32;
 constexpr int MS = 2;                 // keep-bit stages per tile
@@ -438,9 +440,9 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     } else if (warp >= 12) {
         if (DROP) {
             if (KEEP)
-                regs_decrease<32>();
+                regs_decrease<24>();
             else
-                regs_decrease<56>();
+                regs_decrease<32>();
             // keep bits (dropout): thread = row r of both tiles, half m of the keys; for every key
             // tile of the item, in the order the softmax groups consume them, the 64 decisions of
             // the row's keys 64m..64m+63 as two 32-bit words, element (row, key) drawn from its flat
@@ -468,22 +470,23 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                         const int wrow = (q0 + t * BM + (mw % 4) * 32) / 32;
                         uint32_t cw[2] = {0u, 0u};
                         if (KEEP) {
-                            const uint32_t *src = drop.keep_in + keep_word(head, j, wrow, 64 * m + lane, drop.keep_nkt, drop.keep_w);
-                            cw[0] = src[0];
-                            cw[1] = src[32];
+                            const uint32_t *src =
+                                drop.keep_in + keep_word(head, j, wrow, 32 * kMaskWords * m + lane, drop.keep_nkt, drop.keep_w);
+#pragma unroll
+                            for (int q = 0; q < kMaskWords; ++q) cw[q] = src[32 * q];
                         }
                         if (nm[t] >= MS &&
                             !(ok = warp_wait(&bars->mask_empty[t][st], ((nm[t] / MS) + 1) & 1, bars, status)))
                             break;
                         uint32_t w[2];
                         if (KEEP) {
-                            w[0] = warp_transpose_bits32(cw[0], lane);
-                            w[1] = warp_transpose_bits32(cw[1], lane);
+#pragma unroll
+                            for (int q = 0; q < kMaskWords; ++q) w[q] = warp_transpose_bits32(cw[q], lane);
                         } else {
                             const uint64_t row = (uint64_t)(q0 + t * BM + r);
-                            uint64_t g = (((uint64_t)head * S + row) * (uint64_t)S + (uint64_t)(j * BN + 64 * m)) * kDropGolden;
+                            uint64_t g = (((uint64_t)head * S + row) * (uint64_t)S + (uint64_t)(j * BN + 32 * kMaskWords * m)) * kDropGolden;
 #pragma unroll
-                            for (int q = 0; q < 2; ++q) {
+                            for (int q = 0; q < kMaskWords; ++q) {
                                 uint32_t bits = 0u;
 #pragma unroll 4
                                 for (int b = 0; b < 32; ++b) {
@@ -493,24 +496,26 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
                                 w[q] = bits;
                             }
                         }
-                        *reinterpret_cast<uint2 *>(mask_s + ((t * MS + st) * BM + r) * 4 + 2 * m) = make_uint2(w[0], w[1]);
+#pragma unroll
+                        for (int q = 0; q < kMaskWords; ++q) mask_s[((t * MS + st) * BM + r) * 4 + kMaskWords * m + q] = w[q];
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&bars->mask_full[t][st]);
                         ++nm[t];
                         if (!KEEP && drop.keep_out) {
                             // the same decisions kept for the backward: one word per key over this
                             // warp's 32 rows (keep_word), 128 contiguous bytes per store
-                            uint32_t *dst = drop.keep_out + keep_word(head, j, wrow, 64 * m + lane, drop.keep_nkt, drop.keep_w);
-                            dst[0] = warp_transpose_bits32(w[0], lane);
-                            dst[32] = warp_transpose_bits32(w[1], lane);
+                            uint32_t *dst =
+                                drop.keep_out + keep_word(head, j, wrow, 32 * kMaskWords * m + lane, drop.keep_nkt, drop.keep_w);
+#pragma unroll
+                            for (int q = 0; q < kMaskWords; ++q) dst[32 * q] = warp_transpose_bits32(w[q], lane);
                         }
                     }
                 }
             }
         }
     } else {
-        // 640 threads x 96 registers: per lane of a warpgroup 2 x 152 + 56 + 2 x 56 = 472 (drawing),
-        // 2 x 176 + 56 + 2 x 32 = 472 (reading the cache), within 5 x 96 = 480
+        // 896 threads x 72 registers: per lane of a warpgroup 2 x 152 + 56 + 4 x 32 = 488 (drawing),
+        // 2 x 176 + 56 + 4 x 24 = 504 (reading the cache), within 7 x 72 = 504
         if (DROP) {
             if (KEEP)
                 regs_increase<176>();
