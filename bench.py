@@ -531,7 +531,7 @@ def run_ours(args, w):
             "traffic": recorded_traffic("rowdot", w.name)},
         "e2e": e2e,
         "graph": graph,
-        "gpu_launches": launches * K,
+        "gpu_launches": (launches + (1 if fill else 0)) * K,   # + the keep-bit fill kernel with --keep-bits fill
         "clocks": clk.result,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
