@@ -192,10 +192,21 @@ def pin_dropout_keep_known_answers(orc):
     (seed, index) = (0, 0) gives key 0 and h = 0xE220A8397B1DCDAF, so u = 0xE220A8 / 2^24
     = 0.883311...; (0, 1) gives key = gamma, h = 0x6E789E6AA1B965F4, u = 0.431528...;
     (2 gamma, 0) gives key = 2 gamma, h = 0x06C45D188009454F, u = 0.026433...
+    (gamma, 1) gives key = gamma XOR gamma = 0, so the same u as (0, 0) (the sum
+    gamma + gamma would give the u of (2 gamma, 0) instead).
     Each element is kept for p just below its u and dropped for p just above."""
-    for seed, index, u in ((0, 0, 0.8833), (0, 1, 0.43153), ((2 * GOLDEN_GAMMA) % 2 ** 64, 0, 0.026433)):
+    gamma2 = (2 * GOLDEN_GAMMA) % 2 ** 64
+    for seed, index, u in ((0, 0, 0.8833), (0, 1, 0.43153), (gamma2, 0, 0.026433), (GOLDEN_GAMMA, 1, 0.8833)):
         if not orc.keep(seed, index, u - 1e-4) or orc.keep(seed, index, u + 1e-4):
             raise AssertionError(f"keep({seed:#x}, {index}) does not switch at u = {u}")
+    # keep = (u >= p): a rate equal to u itself keeps the element.  Both u below are
+    # 24-bit fractions, exact in fp32; the next fp32 rate above drops it.
+    for seed, index, top24 in ((0, 0, 0xE220A8), (gamma2, 0, 0x06C45D)):
+        u = np.float32(top24) / np.float32(2 ** 24)
+        if not orc.keep(seed, index, float(u)):
+            raise AssertionError(f"keep({seed:#x}, {index}) drops at p = u = {float(u)!r}")
+        if orc.keep(seed, index, float(np.nextafter(u, np.float32(1.0)))):
+            raise AssertionError(f"keep({seed:#x}, {index}) keeps just above p = u")
 
 
 def pin_dropout_keep_rate(orc, n=1 << 15, seed=0xC0FFEE):

@@ -34,6 +34,25 @@ MUTANTS = {
     "keep test reversed": ("return u >= p;", "return u < p;"),
     "keep from the low bits": ("(float)(h >> 40)", "(float)(h & 0xFFFFFF)"),
     "bit-mix constant": ("z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;", "z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B8ull;"),
+    "second bit-mix constant": ("* 0x94D049BB133111EBull;", "* 0x94D049BB133111EAull;"),
+    "second shift 27 -> 26": ("z = (z ^ (z >> 27))", "z = (z ^ (z >> 26))"),
+    "golden increment dropped": ("uint64_t z = x + 0x9E3779B97F4A7C15ull;", "uint64_t z = x;"),
+    "final xor-shift dropped": ("return z ^ (z >> 31);", "return z;"),
+    "seed added, not xored": ("seed ^ (index * 0x9E3779B97F4A7C15ull)", "seed + (index * 0x9E3779B97F4A7C15ull)"),
+    "index not scrambled": ("seed ^ (index * 0x9E3779B97F4A7C15ull)", "seed ^ index"),
+    "keep test strict": ("return u >= p;", "return u > p;"),
+    "u over 2^23": ("/ 16777216.0f", "/ 8388608.0f"),
+    "index base ignored": ("index_base + (uint64_t)(i * S + j)", "(uint64_t)(i * S + j)"),
+    "inverted scale 1 - p": ("1.0 / (1.0 - (double)p)", "(1.0 - (double)p)"),
+    "softmax row term from the dropped P": ("const double *prow = P + i * S;", "const double *prow = (C ? Pd : P) + i * S;"),
+    # plain path
+    "L in log2": ("lse[i] = m + log(z);", "lse[i] = m + log2(z);"),
+    "running max not subtracted": ("row[j] = exp(row[j] - m);", "row[j] = exp(row[j]);"),
+    "row term without P": ("dot += drow[j] * prow[j];", "dot += drow[j];"),
+    "dP uses K instead of V": ("matmul_nt(dout, v, S, hd, dP);", "matmul_nt(dout, k, S, hd, dP);"),
+    "dK uses K instead of Q": ("matmul_tn(dP, q, S, hd, dk);", "matmul_tn(dP, k, S, hd, dk);"),
+    "dS transposed in dQ": ("matmul_nn(dP, k, S, hd, dq);", "matmul_tn(dP, k, S, hd, dq);"),
+    "scale applied twice": ("s[i * S + j] = scale * acc;", "s[i * S + j] = scale * scale * acc;"),
 }
 
 
