@@ -17,12 +17,12 @@ constexpr uint64_t kDropGolden = 0x9E3779B97F4A7C15ull;
 
 constexpr uint64_t kDropMix1 = 0xBF58476D1CE4E5B9ull, kDropMix2 = 0x94D049BB133111EBull;
 
-// Top 24 bits of splitmix64(key), on 32-bit halves: z = key + golden; z ^= z >> 30; z *= mix1
-// (low 64 bits: one widening product and two cross products); z ^= z >> 27; then only bits 32-63
-// of z * mix2 are formed (the high half of the low-by-low product plus the two cross products).
-// The draw is bound by the integer multiplier; this form, seven 32-bit multiplies, measured 7 %
-// more draws per clock on GB300 than the 64-bit expression.
-__device__ __forceinline__ uint32_t drop_draw24(uint64_t key)
+// Bits 32-63 of splitmix64(key), whose top 24 bits are the draw, on 32-bit halves: z = key +
+// golden; z ^= z >> 30; z *= mix1 (low 64 bits: one widening product and two cross products);
+// z ^= z >> 27; then only bits 32-63 of z * mix2 are formed (the high half of the low-by-low
+// product plus the two cross products).  The draw is bound by the integer multiplier; this form,
+// seven 32-bit multiplies, measured 7 % more draws per clock on GB300 than the 64-bit expression.
+__device__ __forceinline__ uint32_t drop_mix_hi32(uint64_t key)
 {
     const uint64_t z0 = key + kDropGolden;
     uint32_t lo = (uint32_t)z0, hi = (uint32_t)(z0 >> 32);
@@ -35,15 +35,16 @@ __device__ __forceinline__ uint32_t drop_draw24(uint64_t key)
     }
     lo ^= __funnelshift_r(lo, hi, 27);
     hi ^= hi >> 27;
-    const uint32_t top = __umulhi(lo, (uint32_t)kDropMix2) + lo * (uint32_t)(kDropMix2 >> 32) + hi * (uint32_t)kDropMix2;
-    return top >> 8;
+    return __umulhi(lo, (uint32_t)kDropMix2) + lo * (uint32_t)(kDropMix2 >> 32) + hi * (uint32_t)kDropMix2;
 }
 
 // Keep decision of the element whose flat index times the golden ratio (mod 2^64) is
 // idx_golden; kernels step idx_golden by a constant along a row instead of multiplying.
+// draw = hi32 >> 8 >= keep_thr  <=>  hi32 >= keep_thr * 2^8, exact since keep_thr < 2^24 (p < 1):
+// the shift moves to the loop-invariant threshold.
 __device__ __forceinline__ bool drop_keep(uint64_t seed, uint64_t idx_golden, uint32_t keep_thr)
 {
-    return drop_draw24(seed ^ idx_golden) >= keep_thr;
+    return drop_mix_hi32(seed ^ idx_golden) >= (keep_thr << 8);
 }
 
 // Cached keep bits (see DropParams): bit i of word keep_word(b, kt, w, c) is the decision of
