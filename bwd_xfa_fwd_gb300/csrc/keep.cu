@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(512) keep_fill_kernel(uint32_t *__restrict__ k
         const int w = 4 * chunk + (int)threadIdx.y;
         uint64_t g = (((uint64_t)b * S + 32u * (uint64_t)w) * (uint64_t)S + key) * kDropGolden;
         uint32_t bits = 0u;
-#pragma unroll 4
+#pragma unroll
         for (int i = 0; i < 32; ++i) {
             bits |= (uint32_t)drop_keep(seed, g, keep_thr) << i;
             g += step;

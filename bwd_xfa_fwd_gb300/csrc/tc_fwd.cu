@@ -488,7 +488,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
 #pragma unroll
                             for (int q = 0; q < kMaskWords; ++q) {
                                 uint32_t bits = 0u;
-#pragma unroll 4
+#pragma unroll
                                 for (int b = 0; b < 32; ++b) {
                                     bits |= (uint32_t)drop_keep(drop.seed, g, drop.keep_thr) << b;
                                     g += kDropGolden;
